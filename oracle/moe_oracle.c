@@ -1,0 +1,378 @@
+/*
+ * Plain CPU oracle of the DeepSeekMoE FP8 layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this file (through oracle/oracle.py).  The CUDA
+ * library never includes, links or calls it, and the two share no code.
+ * Build: gcc -O2 -fno-fast-math -ffp-contract=off -shared -fPIC -lm.
+ *
+ * Every step is written out the plain way, in the order the pages give it,
+ * single-threaded and slow on purpose.  Sources (web pages summarising the
+ * DeepSeek-V3 technical report):
+ *   [TH]  "รายงานเชิงเทคนิคของ DeepSeek-V3" (xyznot.com/th/paper/2412.19437):
+ *         Method §2 "DeepSeekMoE with auxiliary-loss-free balancing" -- the
+ *         equations for h'_t, s_{i,t} and g'_{i,t}, and the bias update rule;
+ *         Key ideas, FP8 bullet -- E4M3 on all tensors, 1x128 activation
+ *         tiles, 128x128 weight blocks, promotion to FP32 every N_c = 128.
+ *   [YLY] "官方揭秘DeepSeek-V3模型训练全流程" (youleyou.com): §2.2 DeepSeekMoE
+ *         (no token dropping); §4.3 FP8 训练 (fine-grained quantisation,
+ *         increased accumulation precision, online max-abs quantisation).
+ *   [DB]  "Deepseek V3 国货之光 开源之光" (databean.com.cn): section
+ *         "Auxiliary-Loss-Free Load Balancing" (the bias only steers top-K;
+ *         gates are the normalised unbiased scores).
+ *   [SYH] "DeepSeek V3技術報告" (sheng-yao-huang.com): section "FP8 資料格式
+ *         訓練", item 1 (map the block max to the format max).
+ *
+ * Readings taken where the pages leave a step open (each one is a choice,
+ * not something the pages print):
+ *   R1  E4M3 is OCP FP8 E4M3FN; encoding rounds to nearest, ties to even,
+ *       and saturates to +-448.
+ *   R2  tile scale = amax / 448 (float32 division); code = enc(x / scale)
+ *       (float32 division, then R1); a tile with amax = 0 gets scale 1.0 and
+ *       all codes 0x00.
+ *   R3  logits accumulate in double and round once to float; sigmoid is
+ *       evaluated in double and rounded to float; the biased score z = s + b
+ *       is a float32 add.
+ *   R4  top-K orders by descending z; equal z: lower expert index first.
+ *       A token is flagged "near tie" when z_(K) - z_(K+1) < 1e-6.
+ *   R5  gate g_k = s_k / sum of the selected s (sum and quotient in double,
+ *       rounded once to float).
+ *   R6  dispatch rows of one expert are in ascending token order; offsets
+ *       are the exclusive scan of the per-expert counts.
+ *   R7  one 128-wide K slab of a block-scaled GEMM is summed exactly (double)
+ *       and rounded once to float; it is promoted with
+ *       acc = fmaf(partial, sa * sw, acc), sa * sw a float32 product.
+ *   R8  SiLU(x) = x / (1 + exp(-x)) in float32; h = SiLU(G) * U; h is
+ *       quantised per 1x128 tile along I before the down projection.
+ *   R9  h'_t = u_t + sum_s y_s + sum_k g_k y_k, summed in double, output float.
+ *   R10 bias update: with n = T*K selections, expert e is overloaded when
+ *       c_e * E > n and underloaded when c_e * E < n (integer compare);
+ *       b_e -= gamma or += gamma in float32; equal load leaves b_e unchanged.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* E4M3 codec (R1)                                                      */
+/* ------------------------------------------------------------------ */
+
+/* Decode one E4M3FN code: sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent 0 is subnormal (m * 2^-9); S.1111.111 is NaN; no infinity. */
+double orc_e4m3_decode(uint8_t code) {
+    int sign = code >> 7;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = m * ldexp(1.0, -9);
+    else
+        mag = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Magnitudes of the 127 finite non-negative codes 0x00..0x7E, increasing. */
+static double g_mag[127];
+static int g_mag_ready = 0;
+
+static void init_mag(void) {
+    if (g_mag_ready) return;
+    for (int c = 0; c < 127; ++c) g_mag[c] = orc_e4m3_decode((uint8_t)c);
+    g_mag_ready = 1;
+}
+
+/* Encode: nearest finite magnitude, ties to the even code, saturating. */
+uint8_t orc_e4m3_encode(float x) {
+    init_mag();
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= g_mag[126]) return sign | 126; /* saturate to 448 */
+    /* largest code lo with g_mag[lo] <= a (binary search on the table) */
+    int lo = 0, hi = 126;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (g_mag[mid] <= a) lo = mid; else hi = mid;
+    }
+    double dlo = a - g_mag[lo], dhi = g_mag[lo + 1] - a;
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = lo + 1;
+    else c = (lo % 2 == 0) ? lo : lo + 1;
+    return sign | (uint8_t)c;
+}
+
+/* Value of every code, filled once from orc_e4m3_decode (used by the GEMM). */
+static double g_dec[256];
+static int g_dec_ready = 0;
+
+static void init_dec(void) {
+    if (g_dec_ready) return;
+    for (int c = 0; c < 256; ++c) g_dec[c] = orc_e4m3_decode((uint8_t)c);
+    g_dec_ready = 1;
+}
+
+void orc_e4m3_encode_array(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(x[i]);
+}
+
+static float bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ------------------------------------------------------------------ */
+/* Fine-grained quantisation (R2): [TH] Key ideas FP8; [YLY] §4.3        */
+/* ------------------------------------------------------------------ */
+
+/* Quantise n values of one tile with a shared scale. */
+static float quant_tile(const float* x, int n, int stride, uint8_t* q, int qstride) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(x[(int64_t)i * stride]);
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        for (int i = 0; i < n; ++i) q[(int64_t)i * qstride] = 0x00;
+        return 1.0f;
+    }
+    float scale = amax / 448.0f;
+    for (int i = 0; i < n; ++i) {
+        float v = x[(int64_t)i * stride] / scale;
+        q[(int64_t)i * qstride] = orc_e4m3_encode(v);
+    }
+    return scale;
+}
+
+/* Activations: one scale per 1x128 tile of a row.  x float32 [M, D];
+ * q [M, D]; scales [M, D/128] (row-major, oracle's own layout). */
+void orc_quant_1x128_f32(const float* x, int M, int D, uint8_t* q, float* scales) {
+    int nb = D / 128;
+    for (int r = 0; r < M; ++r)
+        for (int b = 0; b < nb; ++b)
+            scales[(int64_t)r * nb + b] =
+                quant_tile(x + (int64_t)r * D + b * 128, 128, 1, q + (int64_t)r * D + b * 128, 1);
+}
+
+/* Same for a bfloat16 input (each value widened exactly to float32). */
+void orc_quant_1x128_bf16(const uint16_t* x, int M, int D, uint8_t* q, float* scales) {
+    float* row = (float*)malloc(sizeof(float) * (size_t)D);
+    int nb = D / 128;
+    for (int r = 0; r < M; ++r) {
+        for (int j = 0; j < D; ++j) row[j] = bf16_to_f32(x[(int64_t)r * D + j]);
+        for (int b = 0; b < nb; ++b)
+            scales[(int64_t)r * nb + b] =
+                quant_tile(row + b * 128, 128, 1, q + (int64_t)r * D + b * 128, 1);
+    }
+    free(row);
+}
+
+/* Weights: one scale per 128x128 block.  w float32 [R, C]; q [R, C];
+ * scales [R/128, C/128]. */
+void orc_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales) {
+    int rb = R / 128, cb = C / 128;
+    float* blk = (float*)malloc(sizeof(float) * 128 * 128);
+    uint8_t* qb = (uint8_t*)malloc(128 * 128);
+    for (int i = 0; i < rb; ++i)
+        for (int j = 0; j < cb; ++j) {
+            for (int r = 0; r < 128; ++r)
+                for (int c = 0; c < 128; ++c)
+                    blk[r * 128 + c] = w[(int64_t)(i * 128 + r) * C + j * 128 + c];
+            scales[(int64_t)i * cb + j] = quant_tile(blk, 128 * 128, 1, qb, 1);
+            for (int r = 0; r < 128; ++r)
+                for (int c = 0; c < 128; ++c)
+                    q[(int64_t)(i * 128 + r) * C + j * 128 + c] = qb[r * 128 + c];
+        }
+    free(blk);
+    free(qb);
+}
+
+/* ------------------------------------------------------------------ */
+/* Block-scaled FP8 GEMM with FP32 promotion every 128 (R7)              */
+/* [TH] Key ideas FP8 (N_c = 128); [YLY] §4.3 increased accumulation       */
+/* ------------------------------------------------------------------ */
+
+/* out[m, n] = sum over K slabs of (exact slab dot product) * sa * sw,
+ * accumulated in float32 with fmaf.
+ *   qa [M, Kd] codes, sa [M, Kd/128];  qw [N, Kd] codes, sw [N/128, Kd/128]. */
+void orc_gemm_fp8(const uint8_t* qa, const float* sa, int M, int Kd,
+                  const uint8_t* qw, const float* sw, int N, float* out) {
+    int kb_n = Kd / 128;
+    init_dec();
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int kb = 0; kb < kb_n; ++kb) {
+                double p = 0.0;
+                for (int k = kb * 128; k < kb * 128 + 128; ++k)
+                    p += g_dec[qa[(int64_t)m * Kd + k]] * g_dec[qw[(int64_t)n * Kd + k]];
+                float s = sa[(int64_t)m * kb_n + kb] * sw[(int64_t)(n / 128) * kb_n + kb];
+                acc = fmaf((float)p, s, acc);
+            }
+            out[(int64_t)m * N + n] = acc;
+        }
+}
+
+/* One expert FFN on quantised activation rows (R7, R8).
+ *   qa [M, d], sa [M, d/128]; wg, wu [I, d] with sg, su [I/128, d/128];
+ *   wd [d, I] with sd [d/128, I/128]; y [M, d] float32.                    */
+void orc_expert_ffn(const uint8_t* qa, const float* sa, int M, int d, int I,
+                    const uint8_t* wg, const float* sg, const uint8_t* wu, const float* su,
+                    const uint8_t* wd, const float* sd, float* y) {
+    float* G = (float*)malloc(sizeof(float) * (size_t)M * I);
+    float* U = (float*)malloc(sizeof(float) * (size_t)M * I);
+    uint8_t* qh = (uint8_t*)malloc((size_t)M * I);
+    float* sh = (float*)malloc(sizeof(float) * (size_t)M * (I / 128));
+    orc_gemm_fp8(qa, sa, M, d, wg, sg, I, G);
+    orc_gemm_fp8(qa, sa, M, d, wu, su, I, U);
+    for (int64_t i = 0; i < (int64_t)M * I; ++i) {
+        float g = G[i];
+        float silu = g / (1.0f + expf(-g));
+        G[i] = silu * U[i]; /* G now holds h */
+    }
+    orc_quant_1x128_f32(G, M, I, qh, sh);
+    orc_gemm_fp8(qh, sh, M, I, wd, sd, d, y);
+    free(G); free(U); free(qh); free(sh);
+}
+
+/* ------------------------------------------------------------------ */
+/* Router (R3, R4, R5): [TH] §2 equations for s_{i,t} and g'_{i,t};      */
+/* [DB] "Auxiliary-Loss-Free Load Balancing"                             */
+/* ------------------------------------------------------------------ */
+
+/* For each token t: s_i = sigmoid(u_t . e_i); top-K of z_i = s_i + b_i;
+ * gates = selected s normalised to sum 1.
+ *   u bf16 [T, d]; cent [E, d]; bias [E];  outputs idx, gate [T, K],
+ *   tie [T] (1 = near tie at the K/K+1 boundary), counts [E] (may be NULL),
+ *   scores [T, E] (s values, may be NULL). */
+void orc_route(const uint16_t* u, const float* cent, const float* bias,
+               int T, int d, int E, int K,
+               int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* scores) {
+    float* s = (float*)malloc(sizeof(float) * (size_t)E);
+    float* z = (float*)malloc(sizeof(float) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (counts) memset(counts, 0, sizeof(int32_t) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        for (int i = 0; i < E; ++i) {
+            double l = 0.0;
+            for (int j = 0; j < d; ++j)
+                l += (double)bf16_to_f32(u[(int64_t)t * d + j]) * (double)cent[(int64_t)i * d + j];
+            float lf = (float)l;
+            s[i] = (float)(1.0 / (1.0 + exp(-(double)lf)));
+            z[i] = s[i] + bias[i];
+            taken[i] = 0;
+            if (scores) scores[(int64_t)t * E + i] = s[i];
+        }
+        /* Selection: K+1 passes of "largest z, lowest index on equality". */
+        float zk = 0.0f, zk1 = 0.0f;
+        double ssum = 0.0;
+        for (int k = 0; k < K + 1 && k < E; ++k) {
+            int best = -1;
+            for (int i = 0; i < E; ++i) {
+                if (taken[i]) continue;
+                if (best < 0 || z[i] > z[best]) best = i;
+            }
+            taken[best] = 1;
+            if (k < K) {
+                idx[(int64_t)t * K + k] = best;
+                ssum += (double)s[best];
+                if (k == K - 1) zk = z[best];
+                if (counts) counts[best] += 1;
+            } else {
+                zk1 = z[best];
+            }
+        }
+        for (int k = 0; k < K; ++k)
+            gate[(int64_t)t * K + k] = (float)((double)s[idx[(int64_t)t * K + k]] / ssum);
+        tie[t] = (K < E && (zk - zk1) < 1e-6f) ? 1 : 0;
+    }
+    free(s); free(z); free(taken);
+}
+
+/* ------------------------------------------------------------------ */
+/* Dispatch (R6): counting sort of (token, slot) pairs by expert.        */
+/* [YLY] §2.2: no token is dropped, so every pair gets a row.            */
+/* ------------------------------------------------------------------ */
+
+/* counts [E], offsets [E+1], perm_token [T*K] (row -> token),
+ * inv_row [T*K] ((t, k) -> row).  Returns 0, or -1 on an expert index
+ * outside [0, E). */
+int orc_dispatch(const int32_t* idx, int T, int K, int E,
+                 int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_row) {
+    memset(counts, 0, sizeof(int32_t) * (size_t)E);
+    for (int64_t p = 0; p < (int64_t)T * K; ++p) {
+        if (idx[p] < 0 || idx[p] >= E) return -1;
+        counts[idx[p]] += 1;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int32_t* fill = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    for (int t = 0; t < T; ++t)           /* ascending token order */
+        for (int k = 0; k < K; ++k) {
+            int e = idx[(int64_t)t * K + k];
+            int row = offsets[e] + fill[e]++;
+            perm_token[row] = t;
+            inv_row[(int64_t)t * K + k] = row;
+        }
+    free(fill);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Layer output (R9): [TH] §2 equation for h'_t                          */
+/* ------------------------------------------------------------------ */
+
+/* h'_t for the listed tokens.  Expert weights are passed per group:
+ * groups 0..E-1 are routed, E..E+S-1 shared; a routed group that no listed
+ * token selects may be NULL.  idx, gate [T, K] are the routing of all T
+ * tokens (only the listed rows are read).  out [n_tok, d] float32. */
+void orc_layer_forward(const uint16_t* u, int T, int d, int E, int K, int S, int I,
+                       const int32_t* idx, const float* gate,
+                       const uint8_t* const* wg, const float* const* sg,
+                       const uint8_t* const* wu, const float* const* su,
+                       const uint8_t* const* wd, const float* const* sd,
+                       const int32_t* tok, int n_tok, float* out) {
+    (void)T; /* idx and gate have T rows; only the listed ones are read */
+    uint8_t* qa = (uint8_t*)malloc((size_t)d);
+    float* sa = (float*)malloc(sizeof(float) * (size_t)(d / 128));
+    float* y = (float*)malloc(sizeof(float) * (size_t)d);
+    double* h = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int n = 0; n < n_tok; ++n) {
+        int t = tok[n];
+        const uint16_t* ut = u + (int64_t)t * d;
+        /* the quantised activation is the same for every expert (row-local) */
+        orc_quant_1x128_bf16(ut, 1, d, qa, sa);
+        for (int j = 0; j < d; ++j) h[j] = (double)bf16_to_f32(ut[j]);
+        for (int s = 0; s < S; ++s) {
+            int g = E + s;
+            orc_expert_ffn(qa, sa, 1, d, I, wg[g], sg[g], wu[g], su[g], wd[g], sd[g], y);
+            for (int j = 0; j < d; ++j) h[j] += (double)y[j];
+        }
+        for (int k = 0; k < K; ++k) {
+            int g = idx[(int64_t)t * K + k];
+            orc_expert_ffn(qa, sa, 1, d, I, wg[g], sg[g], wu[g], su[g], wd[g], sd[g], y);
+            double gk = (double)gate[(int64_t)t * K + k];
+            for (int j = 0; j < d; ++j) h[j] += gk * (double)y[j];
+        }
+        for (int j = 0; j < d; ++j) out[(int64_t)n * d + j] = (float)h[j];
+    }
+    free(qa); free(sa); free(y); free(h);
+}
+
+/* ------------------------------------------------------------------ */
+/* Bias update (R10): [TH] §2 update rule (gamma = 0.001 there);         */
+/* [DB] "Auxiliary-Loss-Free Load Balancing"                             */
+/* ------------------------------------------------------------------ */
+
+void orc_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias) {
+    int64_t n = (int64_t)T * K;
+    for (int e = 0; e < E; ++e) {
+        int64_t load = (int64_t)counts[e] * E;
+        if (load > n) bias[e] = bias[e] - gamma;
+        else if (load < n) bias[e] = bias[e] + gamma;
+    }
+}
