@@ -1,0 +1,260 @@
+// C ABI of libmoefp8.so (declared in include/moe_fp8.h): argument checks,
+// workspace layout and the forward pass as one stream-ordered sequence.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace layout shared by moe_forward, moe_route and moe_permute.
+struct Layout {
+    size_t status, logits, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
+};
+
+Layout layout(int T, int d, int E, int K, int S, int I) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    const size_t M = (size_t)T * (K + S);
+    const size_t nchunks = ((size_t)T + kPermuteChunk - 1) / kPermuteChunk;
+    L.status = take(16);
+    L.logits = take(sizeof(float) * (size_t)T * E);
+    L.hist = take(sizeof(int32_t) * nchunks * E);
+    L.base = take(sizeof(int32_t) * nchunks * E);
+    L.go = take(sizeof(int32_t) * (size_t)(E + S + 1));
+    L.offsets = take(sizeof(int32_t) * (size_t)(E + 1));
+    L.perm = take(sizeof(int32_t) * (size_t)T * K);
+    L.inv_row = take(sizeof(int32_t) * (size_t)T * K);
+    L.A = take(M * d);
+    L.sa = take(sizeof(float) * M * (d / 128));
+    L.H = take(M * I);
+    L.sh = take(sizeof(float) * M * (I / 128));
+    L.Y = take(sizeof(uint16_t) * M * d);
+    L.total = off;
+    return L;
+}
+
+int check_layer(const moe_layer_t* L) {
+    if (!L) return MOE_ERR_INVALID_ARG;
+    if (L->d <= 0 || L->E <= 0 || L->K <= 0 || L->S < 0 || L->I <= 0) return MOE_ERR_INVALID_ARG;
+    if (L->E > kMaxExperts || L->K > kMaxTopK || L->K > L->E) return MOE_ERR_INVALID_ARG;
+    if (L->d % 128 || L->I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (L->E + L->S > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!L->centroids || !L->bias || !L->w_gate || !L->w_up || !L->w_down || !L->s_gate ||
+        !L->s_up || !L->s_down)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(L->centroids) || !aligned16(L->w_gate) || !aligned16(L->w_up) ||
+        !aligned16(L->w_down))
+        return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+inline cudaStream_t S_(void* s) { return static_cast<cudaStream_t>(s); }
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return MOE_ERR_CUDA;
+}
+
+int check_launch() {
+    note_launch();
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "GEMM pipeline wait timed out";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_BAD_INDEX: return "index out of range in device data";
+        default: return "unknown status";
+    }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t moe_workspace_size(const moe_layer_t* L, int T_max) {
+    if (!L || T_max < 0 || L->d <= 0 || L->E <= 0 || L->K <= 0 || L->S < 0 || L->I <= 0) return 0;
+    return layout(T_max, L->d, L->E, L->K, L->S, L->I).total;
+}
+
+int moe_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather_rows, int M, int d,
+                    uint8_t* q, float* scales, int scale_ld, int32_t* status, void* stream) {
+    if (M < 0 || n_src < 0 || d <= 0 || scale_ld < M) return MOE_ERR_INVALID_ARG;
+    if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return MOE_OK;
+    if (!x || !q || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q)) return MOE_ERR_MISALIGNED;
+    return launch_quant_1x128(x, n_src, gather_rows, M, M, 1, d, q, scales, scale_ld, status,
+                              S_(stream));
+}
+
+int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, void* stream) {
+    if (R < 0 || C < 0) return MOE_ERR_INVALID_ARG;
+    if (R % 128 || C % 128 || R / 128 > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (R == 0 || C == 0) return MOE_OK;
+    if (!w || !q || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q)) return MOE_ERR_MISALIGNED;
+    return launch_quant_128x128(w, R, C, q, scales, S_(stream));
+}
+
+int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
+              int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
+              void* ws, size_t ws_bytes, void* stream) {
+    if (T < 0 || d <= 0 || E <= 0 || K <= 0 || K > E || K > kMaxTopK || E > kMaxExperts)
+        return MOE_ERR_INVALID_ARG;
+    if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!counts || !centroids || !bias) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!u || !topk_idx || !topk_gate || !tie_flag || !ws)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(centroids) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < sizeof(float) * (size_t)T * E) return MOE_ERR_WORKSPACE;
+    return launch_route(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
+                        static_cast<float*>(ws), S_(stream));
+}
+
+int moe_permute(const int32_t* topk_idx, int T, int K, int E, int32_t* offsets,
+                int32_t* perm_token, int32_t* inv_row, int32_t* status, void* ws,
+                size_t ws_bytes, void* stream) {
+    if (T < 0 || K <= 0 || E <= 0 || K > E || K > kMaxTopK || E > kMaxExperts)
+        return MOE_ERR_INVALID_ARG;
+    if (!offsets || !ws || (T > 0 && (!topk_idx || !perm_token || !inv_row)))
+        return MOE_ERR_INVALID_ARG;
+    const size_t nchunks = ((size_t)T + kPermuteChunk - 1) / kPermuteChunk;
+    const size_t hist_bytes = align_up(sizeof(int32_t) * nchunks * E, 256);
+    if (ws_bytes < 2 * hist_bytes) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    int32_t* hist = static_cast<int32_t*>(ws);
+    int32_t* base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + hist_bytes);
+    return launch_permute(topk_idx, T, K, E, offsets, perm_token, inv_row, nullptr, 0, status,
+                          hist, base, S_(stream));
+}
+
+int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_total,
+                         const int32_t* group_offsets, int G, const uint8_t* W0,
+                         const uint8_t* W1, const float* sw0, const float* sw1, int N, int Kdim,
+                         void* out, float* out_scales, int32_t* status, void* stream) {
+    if (mode != MOE_GEMM_GATE_UP_SILU_QUANT && mode != MOE_GEMM_DOWN) return MOE_ERR_INVALID_ARG;
+    if (M_total < 0 || G < 0 || N <= 0 || Kdim <= 0) return MOE_ERR_INVALID_ARG;
+    if (N % 128 || Kdim % 128 || G > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)G * N > 0x7fffffffLL || (long long)M_total * (N > Kdim ? N : Kdim) > (1LL << 40))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (M_total == 0 || G == 0) return MOE_OK;
+    if (!A || !sa || !group_offsets || !W0 || !sw0 || !out) return MOE_ERR_INVALID_ARG;
+    const bool gu = mode == MOE_GEMM_GATE_UP_SILU_QUANT;
+    if (gu && (!W1 || !sw1 || !out_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(W0) || (gu && !aligned16(W1)) || !aligned16(out))
+        return MOE_ERR_MISALIGNED;
+    return launch_grouped_gemm(mode, A, sa, M_total, group_offsets, G, W0, W1, sw0, sw1, N, Kdim,
+                               out, out_scales, status, S_(stream));
+}
+
+int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
+                const int32_t* inv_row, const uint16_t* Y_shared, int T, int d, int K, int S,
+                float* h_out, void* stream) {
+    if (T < 0 || d <= 0 || K < 0 || K > kMaxTopK || S < 0) return MOE_ERR_INVALID_ARG;
+    if (d % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!u || !h_out || (K > 0 && (!Y || !topk_gate || !inv_row)) || (S > 0 && !Y_shared))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(Y) || !aligned16(Y_shared) || !aligned16(h_out))
+        return MOE_ERR_MISALIGNED;
+    return launch_combine(u, Y, topk_gate, inv_row, Y_shared, T, d, K, S, h_out, S_(stream));
+}
+
+int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
+                float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
+                void* stream) {
+    int rc = check_layer(L);
+    if (rc) return rc;
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (!ws || !counts) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!u || !h_out || !topk_idx || !topk_gate || !tie_flag)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(h_out)) return MOE_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    const int d = L->d, E = L->E, K = L->K, S = L->S, I = L->I, G = E + S;
+    const Layout W = layout(T, d, E, K, S, I);
+    if (ws_bytes < W.total) return MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    const cudaStream_t st = S_(stream);
+    int32_t* status = reinterpret_cast<int32_t*>(base + W.status);
+    float* logits = reinterpret_cast<float*>(base + W.logits);
+    int32_t* hist = reinterpret_cast<int32_t*>(base + W.hist);
+    int32_t* bbase = reinterpret_cast<int32_t*>(base + W.base);
+    int32_t* go = reinterpret_cast<int32_t*>(base + W.go);
+    int32_t* offsets = reinterpret_cast<int32_t*>(base + W.offsets);
+    int32_t* perm = reinterpret_cast<int32_t*>(base + W.perm);
+    int32_t* inv_row = reinterpret_cast<int32_t*>(base + W.inv_row);
+    uint8_t* A = reinterpret_cast<uint8_t*>(base + W.A);
+    float* sa = reinterpret_cast<float*>(base + W.sa);
+    uint8_t* H = reinterpret_cast<uint8_t*>(base + W.H);
+    float* sh = reinterpret_cast<float*>(base + W.sh);
+    uint16_t* Y = reinterpret_cast<uint16_t*>(base + W.Y);
+    const int M = T * (K + S);
+
+    cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((rc = launch_route(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
+                           counts, logits, st)))
+        return rc;
+    if (T == 0) return MOE_OK;
+    if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,
+                             st)))
+        return rc;
+    if ((rc = launch_quant_1x128(u, T, perm, T * K, T, M, d, A, sa, M, status, st))) return rc;
+    if ((rc = launch_grouped_gemm(MOE_GEMM_GATE_UP_SILU_QUANT, A, sa, M, go, G, L->w_gate,
+                                  L->w_up, L->s_gate, L->s_up, I, d, H, sh, status, st)))
+        return rc;
+    if ((rc = launch_grouped_gemm(MOE_GEMM_DOWN, H, sh, M, go, G, L->w_down, nullptr, L->s_down,
+                                  nullptr, d, I, Y, nullptr, status, st)))
+        return rc;
+    return launch_combine(u, Y, topk_gate, inv_row, Y + (size_t)T * K * d, T, d, K, S, h_out, st);
+}
+
+int moe_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,
+                    void* stream) {
+    if (E <= 0 || T < 0 || K <= 0 || !counts || !bias) return MOE_ERR_INVALID_ARG;
+    return launch_update_bias(counts, E, T, K, gamma, bias, S_(stream));
+}
+
+int moe_check_device_status(int32_t* status, void* stream) {
+    if (!status) return MOE_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, status, sizeof(v), cudaMemcpyDeviceToHost, S_(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(S_(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        e = cudaMemsetAsync(status, 0, sizeof(int32_t), S_(stream));
+        if (e == cudaSuccess) e = cudaStreamSynchronize(S_(stream));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return v;
+}
+
+}  // extern "C"

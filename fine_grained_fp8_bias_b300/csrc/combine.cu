@@ -1,0 +1,85 @@
+// Layer output and bias update.
+//
+// Source: "รายงานเชิงเทคนิคของ DeepSeek-V3" (xyznot.com/th/paper/2412.19437),
+// Method §2: h'_t = u_t + sum_{i <= N_s} FFN_i^(s)(u_t) + sum_{i <= N_r}
+// g_{i,t} FFN_i^(r)(u_t); and the end-of-step rule b_i <- b_i - gamma for an
+// overloaded expert, b_i <- b_i + gamma for an underloaded one.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], uint4 raw, float w) {
+    const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(v[i] & 0xFFFFu)), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, bf16_bits_to_float(static_cast<uint16_t>(v[i] >> 16)), acc[2 * i + 1]);
+    }
+}
+
+// One block per token (grid-stride); each thread owns 8 consecutive columns
+// per step.  Sum order: u, shared experts, routed experts by slot.
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ u,
+                                                      const uint16_t* __restrict__ Y,
+                                                      const float* __restrict__ gate,
+                                                      const int32_t* __restrict__ inv_row,
+                                                      const uint16_t* __restrict__ Ysh, int T,
+                                                      int d, int K, int S,
+                                                      float* __restrict__ h) {
+    __shared__ int rows[kMaxTopK];
+    __shared__ float gs[kMaxTopK];
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < K) {
+            rows[threadIdx.x] = inv_row[(size_t)t * K + threadIdx.x];
+            gs[threadIdx.x] = gate[(size_t)t * K + threadIdx.x];
+        }
+        __syncthreads();
+        for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+            float acc[8];
+            const uint4 ur = *reinterpret_cast<const uint4*>(u + (size_t)t * d + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            add_bf16x8(acc, ur, 1.0f);
+            for (int s = 0; s < S; ++s)
+                add_bf16x8(acc, *reinterpret_cast<const uint4*>(Ysh + ((size_t)s * T + t) * d + c), 1.0f);
+            for (int k = 0; k < K; ++k)
+                add_bf16x8(acc, *reinterpret_cast<const uint4*>(Y + (size_t)rows[k] * d + c), gs[k]);
+            float4* out = reinterpret_cast<float4*>(h + (size_t)t * d + c);
+            out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+}
+
+__global__ void update_bias_kernel(const int32_t* __restrict__ counts, int E, long long n,
+                                   float gamma, float* __restrict__ bias) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+        const long long load = (long long)counts[e] * E;
+        if (load > n)
+            bias[e] = bias[e] - gamma;
+        else if (load < n)
+            bias[e] = bias[e] + gamma;
+    }
+}
+
+}  // namespace
+
+int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
+                   const uint16_t* Ysh, int T, int d, int K, int S, float* h, cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    int threads = 128;
+    while (threads < 256 && threads * 8 < d) threads *= 2;
+    const int blocks = T < 148 * 16 ? T : 148 * 16;
+    combine_kernel<<<blocks, threads, 0, st>>>(u, Y, gate, inv_row, Ysh, T, d, K, S, h);
+    return check_launch();
+}
+
+int launch_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,
+                       cudaStream_t st) {
+    update_bias_kernel<<<(E + 255) / 256, 256, 0, st>>>(counts, E, (long long)T * K, gamma, bias);
+    return check_launch();
+}
+
+}  // namespace moe

@@ -1,0 +1,74 @@
+// Shared device helpers and internal launcher declarations of libmoefp8.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe_fp8.h"
+
+namespace moe {
+
+// Counts every kernel this library launches (reported by moe_kernel_launches).
+void note_launch();
+// Records a failed CUDA call for moe_last_cuda_error and returns MOE_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+// Checks the launch that was just made.
+int check_launch();
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Two float32 -> two E4M3 codes, round to nearest even, saturating to +-448
+// (the hardware conversion of sm_89+; `lo` ends up in the low byte).
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Quantise 4 values with one tile scale (IEEE division, as the scale rule).
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float scale) {
+    uint32_t lo = e4m3x2(__fdiv_rn(a, scale), __fdiv_rn(b, scale));
+    uint32_t hi = e4m3x2(__fdiv_rn(c, scale), __fdiv_rn(d, scale));
+    return lo | (hi << 16);
+}
+
+// Tile scale from the tile's max |x|: amax / 448, or 1 for an all-zero tile.
+__device__ __forceinline__ float tile_scale(float amax) {
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+}
+
+__device__ __forceinline__ void flag_status(int32_t* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- launchers
+int launch_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather, int n_gather,
+                       int tail_T, int M, int d, uint8_t* q, float* scales, int scale_ld,
+                       int32_t* status, cudaStream_t st);
+int launch_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, cudaStream_t st);
+int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
+                 int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
+                 cudaStream_t st);
+int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
+                   int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
+                   int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);
+int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
+                        const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
+                        const float* sw0, const float* sw1, int N, int Kdim, void* out,
+                        float* out_scales, int32_t* status, cudaStream_t st);
+int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
+                   const uint16_t* Ysh, int T, int d, int K, int S, float* h, cudaStream_t st);
+int launch_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,
+                       cudaStream_t st);
+
+constexpr int kPermuteChunk = 64;   // tokens per block in the dispatch kernels
+constexpr int kMaxGroups = 1088;    // E + S limit of the grouped GEMM
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace moe

@@ -1,0 +1,581 @@
+// Grouped block-scaled FP8 GEMM for the expert FFNs, on sm_103a tensor cores.
+//
+// Source: "รายงานเชิงเทคนิคของ DeepSeek-V3" (xyznot.com/th/paper/2412.19437),
+// Key ideas, FP8 bullet, and "官方揭秘DeepSeek-V3模型训练全流程"
+// (youleyou.com) §4.3: operands are E4M3 with one FP32 scale per 1x128
+// activation tile and per 128x128 weight block; the tensor core sums one
+// N_c = 128 slab of K, and that partial is promoted to an FP32 accumulator:
+//     acc = fma(partial, sa[row, kb] * sw[nb, kb], acc).
+// The pages do this on H800 by copying the tensor-core result into CUDA-core
+// registers.  Here the slab partial lands in TMEM (two ping-pong buffers);
+// epilogue warps read it with tcgen05.ld and promote it in registers while
+// the tensor core fills the other buffer.
+//
+// Kernel shape (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile [128 x 128] + B tile [256 x 128] per slab,
+//               STAGES-deep shared-memory ring, 128-byte swizzle.
+//   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma.kind::f8f6f4
+//               (M=128, N=256, K=32) per slab into TMEM buffer (slab & 1).
+//   warps 2..9  epilogue, two warpgroups; TMEM lane quarter = warp % 4, so
+//               thread (warp, lane) owns output row 32 * (warp % 4) + lane of
+//               the tile; warpgroup 0 / 1 own half of the 256 columns each.
+// Output tile = 128 rows x 256 columns: in GATE_UP mode 128 gate columns and
+// the 128 up columns of the same intermediate indices (so SiLU(G) * U and
+// the 1x128 re-quantisation of h stay inside one tile), in DOWN mode 256
+// consecutive output features.
+//
+// Tiles are enumerated group-major, then N tile, then M tile: CTAs running
+// at the same time share the weight slab of one (group, N tile) and the A
+// rows of one group through L2, so each weight byte is read from HBM once.
+//
+// Every wait is bounded (about 2 s); on expiry the kernel records
+// MOE_ERR_TIMEOUT in the status word, every role stops, in-flight copies and
+// MMAs are waited for (again bounded) and TMEM is released before exit.
+#include <cuda.h>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int SMEM_A = BM * BK;                 // 16 KB
+constexpr int SMEM_B = BN * BK;                 // 32 KB
+constexpr int SMEM_STAGE = SMEM_A + SMEM_B;     // 48 KB
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr uint32_t TMEM_COLS = 512;             // 2 buffers x 256 fp32 columns
+constexpr unsigned long long WAIT_NS = 2000000000ull;
+
+struct alignas(16) Ctl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t xbar;                              // amax exchange between the epilogue warpgroups
+    uint32_t tmem_base;
+    int abort;
+    int total_tiles;
+    int pad;
+    float amax_x[2][2][BM];                     // [tile parity][warpgroup][row]
+    int go[kMaxGroups + 1];                     // group row offsets
+    int tile_start[kMaxGroups + 1];             // first tile of each group
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * SMEM_STAGE + sizeof(Ctl);
+
+struct Params {
+    int mode;
+    int M_total;
+    int G;
+    int N;
+    int Kdim;
+    const int32_t* go;
+    const float* sa;
+    const float* sw0;
+    const float* sw1;
+    void* out;
+    float* out_scales;
+    int32_t* status;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete.  Returns false when
+// the wait ran out or another role has aborted.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
+                                       int32_t* status) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = now_ns();
+    for (;;) {
+        if (mbar_test(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+        if (now_ns() - t0 > WAIT_NS) {
+            atomicExch(&ctl->abort, 1);
+            flag_status(status, MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Warp-uniform bounded wait: every lane observes the completed phase before
+// any lane goes on (the epilogue's tcgen05.ld is .sync.aligned), and all
+// lanes agree on giving up.
+__device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
+                                       int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long t0 = now_ns();
+    for (;;) {
+        const bool ready = mbar_test(bar, parity);
+        if (__all_sync(0xffffffffu, ready)) return true;
+        int stop = 0;
+        if (lane == 0) {
+            if (*reinterpret_cast<volatile int*>(&ctl->abort)) {
+                stop = 1;
+            } else if (now_ns() - t0 > WAIT_NS) {
+                atomicExch(&ctl->abort, 1);
+                flag_status(status, MOE_ERR_TIMEOUT);
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+// Wait used on the way out: only bounded by time, ignores the abort flag.
+__device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const unsigned long long t0 = now_ns();
+    while (!mbar_test(bar, parity))
+        if (now_ns() - t0 > WAIT_NS) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024
+// bytes stacked along M/N (stride byte offset 1024), descriptor version 1,
+// layout type 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4: D float32 (bits 4-5 =
+// 1), A and B E4M3 (format 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 16 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ----------------------------------------------------------- tile lookup
+struct Tile {
+    int g, nt, mt;
+};
+
+__device__ __forceinline__ Tile find_tile(const Ctl* ctl, int G, int tile) {
+    int lo = 0, hi = G;                     // tile_start[lo] <= tile < tile_start[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ctl->tile_start[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int m = max(0, ctl->go[lo + 1] - ctl->go[lo]);
+    const int mtiles = (m + BM - 1) / BM;
+    const int local = tile - ctl->tile_start[lo];
+    return Tile{lo, local / mtiles, local % mtiles};
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB0,
+                            const __grid_constant__ CUtensorMap tmB1, const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * SMEM_STAGE);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool gate_up = p.mode == MOE_GEMM_GATE_UP_SILU_QUANT;
+    const int NT = gate_up ? p.N / 128 : (p.N + BN - 1) / BN;
+    const int KB = p.Kdim / BK;
+    const int G = p.G;
+
+    // ---- prologue: barriers, TMEM, tile schedule
+    if (warp == 0) {
+        // tile_start[g] = sum_{g' < g} ceil(m_g' / 128) * NT, one warp scan
+        int carry = 0;
+        for (int base = 0; base <= G; base += 32) {
+            const int g = base + lane;
+            int v = 0;
+            if (g <= G) ctl->go[g] = p.go[g];
+            if (g < G) {
+                const int m = max(0, p.go[g + 1] - p.go[g]);
+                v = (m + BM - 1) / BM * NT;
+            }
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (g <= G) ctl->tile_start[g] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            ctl->total_tiles = ctl->tile_start[G];
+            ctl->abort = 0;
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(&ctl->full[s], 1);
+                mbar_init(&ctl->empty[s], 1);
+            }
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&ctl->tfull[b], 1);
+                mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
+            }
+            mbar_init(&ctl->xbar, NUM_EPI_WARPS);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB0);
+            if (gate_up) tma_prefetch_desc(&tmB1);
+        }
+    } else if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&ctl->tmem_base)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int total_tiles = ctl->total_tiles;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Tile tl = find_tile(ctl, G, tile);
+                const int a_row = ctl->go[tl.g] + tl.mt * BM;
+                int b0_row, b1_row;
+                bool has_b1;
+                if (gate_up) {
+                    b0_row = tl.g * p.N + tl.nt * 128;
+                    b1_row = b0_row;
+                    has_b1 = true;
+                } else {
+                    b0_row = tl.g * p.N + tl.nt * BN;
+                    b1_row = b0_row + 128;
+                    has_b1 = tl.nt * BN + 128 < p.N;
+                }
+                const uint32_t bytes = SMEM_A + 128 * BK * (has_b1 ? 2 : 1);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, ctl, p.status)) { ok = false; break; }
+                    uint8_t* sA = smem + (size_t)s * SMEM_STAGE;
+                    uint8_t* sB = sA + SMEM_A;
+                    mbar_expect_tx(&ctl->full[s], bytes);
+                    tma_load_2d(sA, &tmA, &ctl->full[s], kb * BK, a_row);
+                    tma_load_2d(sB, &tmB0, &ctl->full[s], kb * BK, b0_row);
+                    if (has_b1)
+                        tma_load_2d(sB + 128 * BK, gate_up ? &tmB1 : &tmB0, &ctl->full[s],
+                                    kb * BK, b1_row);
+                }
+            }
+            // make sure no copy is still landing in shared memory when the CTA exits
+            const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0;
+            for (uint32_t j = first; j < it; ++j) mbar_drain(&ctl->full[j % STAGES], (j / STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3(BM, BN);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    const uint32_t buf = it & 1;
+                    const uint32_t tph = (it >> 1) & 1;
+                    if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, ctl, p.status)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->full[s], ph, ctl, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + (size_t)s * SMEM_STAGE);
+                    const uint32_t b0 = a0 + SMEM_A;
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_e4m3(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                                 k > 0 ? 1u : 0u);
+                    mma_commit(&ctl->empty[s]);
+                    mma_commit(&ctl->tfull[buf]);
+                }
+            }
+            // wait for the last MMAs before TMEM is released
+            if (it > 0) mbar_drain(&ctl->tfull[(it - 1) & 1], ((it - 1) >> 1) & 1);
+        }
+    } else {
+        // ================= epilogue =================
+        const int ew = warp - 2;
+        const int wg = ew >> 2;                   // column half
+        const int quarter = warp & 3;             // TMEM lane quarter
+        const int row = quarter * 32 + lane;      // row within the tile
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const int NB = p.N / 128;
+        uint32_t it = 0;
+        int tcount = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
+            const Tile tl = find_tile(ctl, G, tile);
+            const int g0 = ctl->go[tl.g];
+            const int m_g = max(0, ctl->go[tl.g + 1] - g0);
+            const int lrow = tl.mt * BM + row;
+            const int grow = g0 + lrow;
+            const bool valid = lrow < m_g && grow < p.M_total;
+            // weight-scale rows for this thread's column half
+            const float* swa;
+            const float* swb;
+            bool cols_valid = true;
+            if (gate_up) {
+                swa = p.sw0 + ((size_t)tl.g * NB + tl.nt) * KB;
+                swb = p.sw1 + ((size_t)tl.g * NB + tl.nt) * KB;
+            } else {
+                const int nb = tl.nt * 2 + wg;
+                cols_valid = nb < NB;
+                swa = p.sw0 + ((size_t)tl.g * NB + (cols_valid ? nb : 0)) * KB;
+                swb = swa;
+            }
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t buf = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                const float sa = valid ? p.sa[(size_t)kb * p.M_total + grow] : 0.0f;
+                const float s_lo = sa * swa[kb];
+                const float s_hi = sa * swb[kb];
+                if (!warp_wait(&ctl->tfull[buf], tph, ctl, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + lane_addr + buf * BN;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    // GATE_UP: chunks 0-3 = gate cols wg*64 + [0,64), chunks 4-7 = up cols
+                    // 128 + wg*64 + [0,64).  DOWN: cols wg*128 + [0,128).
+                    const int col = gate_up ? (c < 4 ? wg * 64 + c * 16 : 128 + wg * 64 + (c - 4) * 16)
+                                            : wg * 128 + c * 16;
+                    float v[16];
+                    tmem_ld16(tbase + col, v);
+                    const float s = (gate_up && c >= 4) ? s_hi : s_lo;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(v[i], s, acc[c * 16 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            }
+            if (!ok) break;
+            // ---- tile finalisation
+            if (gate_up) {
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float gv = acc[i];
+                    const float h = __fdiv_rn(gv, 1.0f + expf(-gv)) * acc[64 + i];
+                    acc[i] = h;
+                    amax = fmaxf(amax, fabsf(h));
+                }
+                // Exchange the row's amax with the other warpgroup.  One xbar phase per
+                // tile: no warp can arrive for tile n+1 before all arrived for tile n,
+                // and the double-buffered slots keep tile n's values until then.
+                const int par = tcount & 1;
+                ctl->amax_x[par][wg][row] = amax;
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->xbar);
+                if (!warp_wait(&ctl->xbar, (uint32_t)par, ctl, p.status)) { ok = false; break; }
+                amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
+                const float scale = tile_scale(amax);
+                if (valid) {
+                    uint8_t* dst = static_cast<uint8_t*>(p.out) + (size_t)grow * p.N + tl.nt * 128 + wg * 64;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 16) {
+                        uint4 o;
+                        if (amax == 0.0f) {
+                            o = make_uint4(0u, 0u, 0u, 0u);
+                        } else {
+                            o.x = quant4(acc[j + 0], acc[j + 1], acc[j + 2], acc[j + 3], scale);
+                            o.y = quant4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7], scale);
+                            o.z = quant4(acc[j + 8], acc[j + 9], acc[j + 10], acc[j + 11], scale);
+                            o.w = quant4(acc[j + 12], acc[j + 13], acc[j + 14], acc[j + 15], scale);
+                        }
+                        *reinterpret_cast<uint4*>(dst + j) = o;
+                    }
+                    if (wg == 0) p.out_scales[(size_t)tl.nt * p.M_total + grow] = scale;
+                }
+            } else if (valid && cols_valid) {
+                uint16_t* dst = static_cast<uint16_t*>(p.out) + (size_t)grow * p.N + tl.nt * BN + wg * 128;
+#pragma unroll
+                for (int j = 0; j < 128; j += 8) {
+                    uint4 o;
+                    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
+                    __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
+                    __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+                    o.x = *reinterpret_cast<uint32_t*>(&b0);
+                    o.y = *reinterpret_cast<uint32_t*>(&b1);
+                    o.z = *reinterpret_cast<uint32_t*>(&b2);
+                    o.w = *reinterpret_cast<uint32_t*>(&b3);
+                    *reinterpret_cast<uint4*>(dst + j) = o;
+                }
+            }
+        }
+    }
+
+    // ---- teardown: every TMEM read and MMA is finished before the release
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS));
+    }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D uint8 tensor [rows, cols] (cols contiguous), box 128 x 128, 128-byte swizzle.
+int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+}  // namespace
+
+int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
+                        const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
+                        const float* sw0, const float* sw1, int N, int Kdim, void* out,
+                        float* out_scales, int32_t* status, cudaStream_t st) {
+    if (M_total == 0 || G == 0) return MOE_OK;
+    static int sm_count = 0;
+    static std::once_flag once;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::call_once(once, [&] {
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES);
+    });
+    if (sm_count <= 0) return cuda_fail(cudaErrorInvalidDevice);
+    CUtensorMap mA, mB0, mB1;
+    int rc = make_map(&mA, A, (uint64_t)M_total, (uint64_t)Kdim);
+    if (rc) return rc;
+    rc = make_map(&mB0, W0, (uint64_t)G * N, (uint64_t)Kdim);
+    if (rc) return rc;
+    if (mode == MOE_GEMM_GATE_UP_SILU_QUANT) {
+        rc = make_map(&mB1, W1, (uint64_t)G * N, (uint64_t)Kdim);
+        if (rc) return rc;
+    } else {
+        mB1 = mB0;
+    }
+    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status};
+    const int NT = mode == MOE_GEMM_GATE_UP_SILU_QUANT ? N / 128 : (N + BN - 1) / BN;
+    const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NT;
+    const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);
+    grouped_gemm_fp8_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
+    return check_launch();
+}
+
+}  // namespace moe

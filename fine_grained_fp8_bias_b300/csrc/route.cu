@@ -1,0 +1,215 @@
+// Router: affinity logits, sigmoid, bias-steered top-K, gate normalisation.
+//
+// Source: "รายงานเชิงเทคนิคของ DeepSeek-V3" (xyznot.com/th/paper/2412.19437),
+// Method §2: s_{i,t} = Sigmoid(u_t^T e_i); g'_{i,t} = s_{i,t} when
+// s_{i,t} + b_i is among the top K_r of {s_{j,t} + b_j}, else 0; g is g'
+// normalised.  "Deepseek V3 国货之光 开源之光" (databean.com.cn), section
+// "Auxiliary-Loss-Free Load Balancing": the bias b_i only steers which
+// experts are chosen; the gate values use the unbiased s.
+//
+// Two kernels: a float32 GEMM for the logits l = u E^T (CUDA cores, exact
+// products of bf16 x fp32, float32 accumulation), then one warp per token
+// for sigmoid, selection and gates.  Selection order: descending s + b,
+// equal scores broken by the lower expert index.  Near-tie flag: the K-th
+// and (K+1)-th biased scores differ by less than 1e-6.
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int LT = 64;   // tokens per logits tile
+constexpr int LE = 64;   // experts per logits tile
+constexpr int LK = 32;   // d per smem step
+
+// l[t, e] (+)= sum_{j in this block's d-range} u[t, j] * c[e, j].
+// 256 threads, each computing a 4 x 4 patch of the 64 x 64 tile.  With
+// split > 1 (few tokens) every block adds its partial sum atomically into a
+// zeroed l.
+__global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict__ u,
+                                                     const float* __restrict__ c, int T, int d,
+                                                     int E, int split, float* __restrict__ l) {
+    __shared__ __align__(16) float us[LK][LT + 4];
+    __shared__ __align__(16) float cs[LK][LE + 4];
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * LT, e0 = blockIdx.y * LE;
+    const int steps = d / LK;
+    const int s_begin = (int)((long long)steps * blockIdx.z / split);
+    const int s_end = (int)((long long)steps * (blockIdx.z + 1) / split);
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    const int lrow = tid >> 2;          // 0..63: token (or expert) loaded by this thread
+    const int lk = (tid & 3) * 8;       // 8 consecutive k
+    for (int s = s_begin; s < s_end; ++s) {
+        const int k0 = s * LK;
+        {
+            const int t = t0 + lrow;
+            float v[8];
+            if (t < T) {
+                uint4 raw = *reinterpret_cast<const uint4*>(u + (size_t)t * d + k0 + lk);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
+                    v[2 * i + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) us[lk + i][lrow] = v[i];
+        }
+        {
+            const int e = e0 + lrow;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (e < E) {
+                const float4* p = reinterpret_cast<const float4*>(c + (size_t)e * d + k0 + lk);
+                a = p[0];
+                b = p[1];
+            }
+            cs[lk + 0][lrow] = a.x; cs[lk + 1][lrow] = a.y; cs[lk + 2][lrow] = a.z; cs[lk + 3][lrow] = a.w;
+            cs[lk + 4][lrow] = b.x; cs[lk + 5][lrow] = b.y; cs[lk + 6][lrow] = b.z; cs[lk + 7][lrow] = b.w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < LK; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(&us[k][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4*>(&cs[k][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e >= E) continue;
+            if (split > 1)
+                atomicAdd(&l[(size_t)t * E + e], acc[i][j]);
+            else
+                l[(size_t)t * E + e] = acc[i][j];
+        }
+    }
+}
+
+// Larger score first; equal scores: lower expert index first.
+__device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
+    return za > zb || (za == zb && ia < ib);
+}
+
+// One warp per token.  Lane L holds experts L, L + 32, ... (NV per lane).
+template <int NV>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ l,
+                                                   const float* __restrict__ bias, int T, int E,
+                                                   int K, int32_t* __restrict__ idx,
+                                                   float* __restrict__ gate,
+                                                   uint8_t* __restrict__ tie,
+                                                   int32_t* __restrict__ counts) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    float s[NV], z[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int e = j * 32 + lane;
+        if (e < E) {
+            const float x = l[(size_t)t * E + e];
+            s[j] = __fdiv_rn(1.0f, 1.0f + expf(-x));
+            z[j] = s[j] + bias[e];
+        } else {
+            s[j] = 0.0f;
+            z[j] = -FLT_MAX;
+        }
+    }
+    unsigned taken = 0;                 // bit j: my expert j*32+lane already selected
+    float my_s = 0.0f, ssum = 0.0f, zk = 0.0f, zk1 = 0.0f;
+    int my_e = -1;
+    const int rounds = K < E ? K + 1 : K;
+    for (int k = 0; k < rounds; ++k) {
+        float bz = -FLT_MAX;
+        int be = 0x7fffffff, bj = -1;
+        float bs = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if (e < E && !(taken >> j & 1u) && better(z[j], e, bz, be)) {
+                bz = z[j]; be = e; bj = j; bs = s[j];
+            }
+        }
+        float wz = bz, ws = bs;
+        int we = be;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, wz, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, we, off);
+            const float os = __shfl_xor_sync(0xffffffffu, ws, off);
+            if (better(oz, oe, wz, we)) { wz = oz; we = oe; ws = os; }
+        }
+        if (we == be && bj >= 0) taken |= 1u << bj;     // the owner marks it
+        if (k < K) {
+            ssum += ws;                                  // same order in every lane
+            if (lane == k) { my_e = we; my_s = ws; }
+            if (k == K - 1) zk = wz;
+        } else {
+            zk1 = wz;
+        }
+    }
+    if (lane < K) {
+        idx[(size_t)t * K + lane] = my_e;
+        gate[(size_t)t * K + lane] = __fdiv_rn(my_s, ssum);
+        atomicAdd(&counts[my_e], 1);
+    }
+    if (lane == 0) tie[t] = (K < E && (zk - zk1) < 1e-6f) ? 1 : 0;
+}
+
+template <int NV>
+void launch_topk_nv(const float* l, const float* bias, int T, int E, int K, int32_t* idx,
+                    float* gate, uint8_t* tie, int32_t* counts, cudaStream_t st) {
+    const int warps = 8;
+    topk_kernel<NV><<<(T + warps - 1) / warps, warps * 32, 0, st>>>(l, bias, T, E, K, idx, gate,
+                                                                     tie, counts);
+}
+
+}  // namespace
+
+int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
+                 int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
+                 cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (T == 0) return MOE_OK;
+    const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
+    int split = 1;
+    const int target = 2 * 148;
+    while (gx * gy * split < target && split * 2 <= d / LK / 4) split *= 2;
+    if (split > 1) {
+        e = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    logits_kernel<<<dim3(gx, gy, split), 256, 0, st>>>(u, cent, T, d, E, split, logits);
+    int rc = check_launch();
+    if (rc) return rc;
+    const int nv = (E + 31) / 32;
+    if (nv <= 1) launch_topk_nv<1>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 2) launch_topk_nv<2>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 4) launch_topk_nv<4>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 8) launch_topk_nv<8>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 16) launch_topk_nv<16>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    else launch_topk_nv<32>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    return check_launch();
+}
+
+}  // namespace moe

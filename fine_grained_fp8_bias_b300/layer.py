@@ -1,0 +1,88 @@
+"""A DeepSeekMoE FP8 layer held in device memory, driven through the C ABI.
+
+MoELayer owns the layer's device tensors (centroids, bias, E4M3 weight
+stacks and their 128x128 block scales), a workspace, and the output
+buffers of one forward pass.  Quantising the float32 master weights and the
+whole forward run in libmoefp8's kernels; torch only allocates memory.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import lib, workloads
+
+
+class MoELayer:
+    def __init__(self, d: int, E: int, K: int, S: int, I: int, device="cuda"):
+        self.d, self.E, self.K, self.S, self.I = d, E, K, S, I
+        self.G = E + S
+        dev = torch.device(device)
+        self.device = dev
+        self.centroids = torch.zeros((E, d), dtype=torch.float32, device=dev)
+        self.bias = torch.zeros((E,), dtype=torch.float32, device=dev)
+        self.w_gate = torch.zeros((self.G, I, d), dtype=torch.uint8, device=dev)
+        self.w_up = torch.zeros((self.G, I, d), dtype=torch.uint8, device=dev)
+        self.w_down = torch.zeros((self.G, d, I), dtype=torch.uint8, device=dev)
+        self.s_gate = torch.ones((self.G, I // 128, d // 128), dtype=torch.float32, device=dev)
+        self.s_up = torch.ones((self.G, I // 128, d // 128), dtype=torch.float32, device=dev)
+        self.s_down = torch.ones((self.G, d // 128, I // 128), dtype=torch.float32, device=dev)
+        self._ws = None
+        self._T_ws = -1
+
+    # ------------------------------------------------------------ set-up
+    @classmethod
+    def from_config(cls, cfg: workloads.LayerConfig, device="cuda") -> "MoELayer":
+        """Synthetic layer of a workload: seeded centroids, bias and master
+        weights, each weight matrix quantised 128x128 by moe_quant_128x128."""
+        L = cls(cfg.d, cfg.E, cfg.K, cfg.S, cfg.I, device)
+        L.centroids.copy_(workloads.centroids(cfg, L.device))
+        L.bias.copy_(workloads.bias(cfg, L.device))
+        for g in range(L.G):
+            for which, q, s in (("gate", L.w_gate, L.s_gate), ("up", L.w_up, L.s_up),
+                                ("down", L.w_down, L.s_down)):
+                w = workloads.master_weight(cfg, which, g, L.device)
+                lib.moe_quant_128x128(w, q[g], s[g])
+        return L
+
+    def set_group(self, g: int, gate, up, down):
+        """Install already-quantised (codes, scales) pairs for group g."""
+        for (q, s), dq, ds in ((gate, self.w_gate, self.s_gate), (up, self.w_up, self.s_up),
+                               (down, self.w_down, self.s_down)):
+            dq[g].copy_(torch.as_tensor(q))
+            ds[g].copy_(torch.as_tensor(s))
+
+    def struct(self) -> lib.moe_layer_t:
+        return lib.moe_layer_t(self.d, self.E, self.K, self.S, self.I,
+                               self.centroids.data_ptr(), self.bias.data_ptr(),
+                               self.w_gate.data_ptr(), self.w_up.data_ptr(),
+                               self.w_down.data_ptr(), self.s_gate.data_ptr(),
+                               self.s_up.data_ptr(), self.s_down.data_ptr())
+
+    def workspace(self, T: int) -> torch.Tensor:
+        if self._ws is None or self._T_ws < T:
+            n = lib.moe_workspace_size(self.struct(), T)
+            self._ws = torch.empty(n + 256, dtype=torch.uint8, device=self.device)
+            self._T_ws = T
+        return self._ws
+
+    def outputs(self, T: int) -> dict:
+        dev = self.device
+        return {"h": torch.empty((T, self.d), dtype=torch.float32, device=dev),
+                "idx": torch.empty((T, self.K), dtype=torch.int32, device=dev),
+                "gate": torch.empty((T, self.K), dtype=torch.float32, device=dev),
+                "counts": torch.empty((self.E,), dtype=torch.int32, device=dev),
+                "tie": torch.empty((T,), dtype=torch.uint8, device=dev)}
+
+    # ----------------------------------------------------------- forward
+    def forward(self, u: torch.Tensor, out: dict | None = None, stream=None) -> dict:
+        T = u.shape[0]
+        out = self.outputs(T) if out is None else out
+        return lib.moe_forward(self.struct(), u, self.workspace(T), out, stream)
+
+    def update_bias(self, counts: torch.Tensor, T: int, gamma: float, stream=None):
+        lib.moe_update_bias(counts, self.bias, T, self.K, gamma, stream)
+
+    def status(self, stream=None) -> int:
+        """Reads and clears the device status word of the last forward (syncs)."""
+        ws = self._ws
+        return lib.moe_check_device_status(ws[:16].view(torch.int32), stream) if ws is not None else 0

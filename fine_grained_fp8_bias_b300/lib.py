@@ -1,0 +1,243 @@
+"""ctypes binding of libmoefp8.so (include/moe_fp8.h).
+
+Argument marshalling only: every function passes device pointers of torch
+tensors to the C entry point of the same name and raises MoeError on a
+non-zero status.  Every step of the layer runs in the library's CUDA
+kernels; there is no CPU fallback, and importing this module on a machine
+without the built library raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoefp8.so")
+
+MOE_OK = 0
+MOE_GEMM_GATE_UP_SILU_QUANT = 1
+MOE_GEMM_DOWN = 2
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib.moe_status_string(code).decode() if _lib else str(code)
+        if code == -4 and _lib:
+            msg += f" (cudaError {_lib.moe_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{code}]")
+
+
+class moe_layer_t(ctypes.Structure):
+    _fields_ = [("d", I32), ("E", I32), ("K", I32), ("S", I32), ("I", I32),
+                ("centroids", P), ("bias", P), ("w_gate", P), ("w_up", P), ("w_down", P),
+                ("s_gate", P), ("s_up", P), ("s_down", P)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoefp8.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [I32]
+    lib.moe_last_cuda_error.restype = I32
+    lib.moe_kernel_launches.restype = ctypes.c_uint64
+    lib.moe_workspace_size.restype = ctypes.c_size_t
+    lib.moe_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
+    sigs = {
+        "moe_quant_1x128": [P, I32, P, I32, I32, P, P, I32, P, P],
+        "moe_quant_128x128": [P, I32, I32, P, P, P],
+        "moe_route": [P, P, P, I32, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
+        "moe_permute": [P, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
+        "moe_grouped_gemm_fp8": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
+        "moe_combine": [P, P, P, P, P, I32, I32, I32, I32, P, P],
+        "moe_forward": [ctypes.POINTER(moe_layer_t), P, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
+        "moe_update_bias": [P, I32, I32, I32, ctypes.c_float, P, P],
+        "moe_check_device_status": [P, P],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = I32
+        fn.argtypes = args
+    return lib
+
+
+_lib: Optional[ctypes.CDLL] = None
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t.data_ptr()
+
+
+def _dev(t: torch.Tensor, name: str):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def _bits(t: torch.Tensor, dtype) -> torch.Tensor:
+    if t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    return t
+
+
+def kernel_launches() -> int:
+    return int(_lib.moe_kernel_launches())
+
+
+# ------------------------------------------------------------ entry points
+def moe_quant_1x128(x: torch.Tensor, gather_rows: Optional[torch.Tensor] = None,
+                    M: Optional[int] = None, q: Optional[torch.Tensor] = None,
+                    scales: Optional[torch.Tensor] = None, scale_ld: Optional[int] = None,
+                    status: Optional[torch.Tensor] = None, stream=None):
+    """x bf16 [n_src, d] -> (q uint8 [M, d], scales float32 [d/128, scale_ld])."""
+    _bits(x, torch.bfloat16)
+    _dev(x, "x")
+    n_src, d = x.shape
+    M = (gather_rows.numel() if gather_rows is not None else n_src) if M is None else M
+    scale_ld = M if scale_ld is None else scale_ld
+    if q is None:
+        q = torch.empty((M, d), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((d // 128, scale_ld), dtype=torch.float32, device=x.device)
+    _check(_lib.moe_quant_1x128(_ptr(x), n_src, _ptr(gather_rows), M, d, _ptr(q), _ptr(scales),
+                                scale_ld, _ptr(status), _stream(stream)), "moe_quant_1x128")
+    return q, scales
+
+
+def moe_quant_128x128(w: torch.Tensor, q: Optional[torch.Tensor] = None,
+                      scales: Optional[torch.Tensor] = None, stream=None):
+    """w float32 [R, C] -> (q uint8 [R, C], scales float32 [R/128, C/128])."""
+    _bits(w, torch.float32)
+    _dev(w, "w")
+    R, C = w.shape
+    if q is None:
+        q = torch.empty((R, C), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((R // 128, C // 128), dtype=torch.float32, device=w.device)
+    _check(_lib.moe_quant_128x128(_ptr(w), R, C, _ptr(q), _ptr(scales), _stream(stream)),
+           "moe_quant_128x128")
+    return q, scales
+
+
+def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
+              ws: Optional[torch.Tensor] = None, out: Optional[dict] = None, stream=None) -> dict:
+    _bits(u, torch.bfloat16)
+    _dev(u, "u")
+    T, d = u.shape
+    E = centroids.shape[0]
+    dev = u.device
+    if out is None:
+        out = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),
+               "gate": torch.empty((T, K), dtype=torch.float32, device=dev),
+               "tie": torch.empty((T,), dtype=torch.uint8, device=dev),
+               "counts": torch.empty((E,), dtype=torch.int32, device=dev)}
+    if ws is None:
+        ws = torch.empty(max(4 * T * E, 256), dtype=torch.uint8, device=dev)
+    _check(_lib.moe_route(_ptr(u), _ptr(centroids), _ptr(bias), T, d, E, K, _ptr(out["idx"]),
+                          _ptr(out["gate"]), _ptr(out["tie"]), _ptr(out["counts"]), _ptr(ws),
+                          ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+    return out
+
+
+def moe_permute(topk_idx: torch.Tensor, E: int, ws: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    _dev(topk_idx, "topk_idx")
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    out = {"offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
+           "perm_token": torch.empty((T * K,), dtype=torch.int32, device=dev),
+           "inv_row": torch.empty((T, K), dtype=torch.int32, device=dev)}
+    if ws is None:
+        nchunks = (T + 63) // 64
+        ws = torch.empty(2 * ((4 * nchunks * E + 255) // 256 * 256) + 256, dtype=torch.uint8,
+                         device=dev)
+    _check(_lib.moe_permute(_ptr(topk_idx), T, K, E, _ptr(out["offsets"]), _ptr(out["perm_token"]),
+                            _ptr(out["inv_row"]), _ptr(status), _ptr(ws),
+                            ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
+    return out
+
+
+def moe_grouped_gemm_fp8(mode: int, A: torch.Tensor, sa: torch.Tensor,
+                         group_offsets: torch.Tensor, W0: torch.Tensor,
+                         W1: Optional[torch.Tensor], sw0: torch.Tensor,
+                         sw1: Optional[torch.Tensor], out: Optional[torch.Tensor] = None,
+                         out_scales: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None):
+    """A uint8 [M_total, Kdim]; W0/W1 uint8 [G, N, Kdim] -> out (fp8 codes or bf16) [, scales]."""
+    _dev(A, "A")
+    M_total, Kdim = A.shape
+    G, N, _ = W0.shape
+    dev = A.device
+    if out is None:
+        out = torch.empty((M_total, N), dtype=torch.uint8 if mode == MOE_GEMM_GATE_UP_SILU_QUANT
+                          else torch.bfloat16, device=dev)
+    if mode == MOE_GEMM_GATE_UP_SILU_QUANT and out_scales is None:
+        out_scales = torch.empty((N // 128, M_total), dtype=torch.float32, device=dev)
+    _check(_lib.moe_grouped_gemm_fp8(mode, _ptr(A), _ptr(sa), M_total, _ptr(group_offsets), G,
+                                     _ptr(W0), _ptr(W1), _ptr(sw0), _ptr(sw1), N, Kdim, _ptr(out),
+                                     _ptr(out_scales), _ptr(status), _stream(stream)),
+           "moe_grouped_gemm_fp8")
+    return (out, out_scales) if mode == MOE_GEMM_GATE_UP_SILU_QUANT else out
+
+
+def moe_combine(u: torch.Tensor, Y: torch.Tensor, topk_gate: torch.Tensor, inv_row: torch.Tensor,
+                Y_shared: Optional[torch.Tensor], S: int, h: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    T, d = u.shape
+    K = topk_gate.shape[1]
+    if h is None:
+        h = torch.empty((T, d), dtype=torch.float32, device=u.device)
+    _check(_lib.moe_combine(_ptr(u), _ptr(Y), _ptr(topk_gate), _ptr(inv_row), _ptr(Y_shared), T, d,
+                            K, S, _ptr(h), _stream(stream)), "moe_combine")
+    return h
+
+
+def moe_update_bias(counts: torch.Tensor, bias: torch.Tensor, T: int, K: int, gamma: float,
+                    stream=None) -> torch.Tensor:
+    _check(_lib.moe_update_bias(_ptr(counts), counts.numel(), T, K, gamma, _ptr(bias),
+                                _stream(stream)), "moe_update_bias")
+    return bias
+
+
+def moe_check_device_status(status: torch.Tensor, stream=None) -> int:
+    return int(_lib.moe_check_device_status(_ptr(status), _stream(stream)))
+
+
+def moe_workspace_size(layer: moe_layer_t, T: int) -> int:
+    return int(_lib.moe_workspace_size(ctypes.byref(layer), T))
+
+
+def moe_forward(layer: moe_layer_t, u: torch.Tensor, ws: torch.Tensor, out: dict,
+                stream=None) -> dict:
+    """One layer forward into the preallocated tensors of `out` (h, idx, gate, counts, tie)."""
+    T = u.shape[0]
+    _check(_lib.moe_forward(ctypes.byref(layer), _ptr(u), T, _ptr(out["h"]), _ptr(out["idx"]),
+                            _ptr(out["gate"]), _ptr(out["counts"]), _ptr(out["tie"]), _ptr(ws),
+                            ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+    return out

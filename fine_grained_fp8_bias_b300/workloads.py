@@ -29,6 +29,7 @@ import dataclasses
 import math
 from typing import Optional
 
+import numpy as np
 import torch
 
 _M32 = 0xFFFFFFFF
@@ -70,8 +71,29 @@ def stream_key(seed: int, *ids: int) -> tuple[int, int]:
     return k, k2
 
 
+def _lowbias32_np(x: np.ndarray) -> np.ndarray:
+    """lowbias32 on uint32 arrays (numpy wraps uint32 products mod 2^32)."""
+    x = x ^ (x >> np.uint32(16))
+    x = x * np.uint32(0x7FEB352D)
+    x = x ^ (x >> np.uint32(15))
+    x = x * np.uint32(0x846CA68B)
+    x = x ^ (x >> np.uint32(16))
+    return x
+
+
 def _words(key: tuple[int, int], start: int, n: int, per: int, device) -> torch.Tensor:
-    """Hash words for elements [start, start+n), `per` words each -> int64 [n, per]."""
+    """Hash words for elements [start, start+n), `per` words each -> int64 [n, per].
+
+    The CPU path uses numpy uint32 arithmetic, the CUDA path torch int64
+    arithmetic reduced mod 2^32; both compute the same function."""
+    if torch.device(device).type == "cpu":
+        lo = start * per
+        if lo + n * per > 1 << 32:
+            raise ValueError("counter range beyond 2^32 elements")
+        idx = np.arange(lo, lo + n * per, dtype=np.uint32)   # high counter word is 0
+        x = _lowbias32_np(idx ^ np.uint32(key[0]))
+        x = _lowbias32_np(x ^ np.uint32(key[1]))
+        return torch.from_numpy(x.astype(np.int64)).view(n, per)
     idx = torch.arange(start * per, (start + n) * per, dtype=torch.int64, device=device)
     x = _lowbias32((idx & _M32) ^ key[0])
     x = _lowbias32(x ^ ((idx >> 32) * 0x9E3779B9 & _M32) ^ key[1])

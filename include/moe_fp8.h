@@ -1,0 +1,198 @@
+/*
+ * moe_fp8.h -- C ABI of libmoefp8.so: the forward pass of one DeepSeekMoE
+ * layer with auxiliary-loss-free routing and fine-grained FP8 expert GEMMs,
+ * written for NVIDIA B300 (sm_103a).
+ *
+ * Sources (web pages summarising the DeepSeek-V3 technical report):
+ *   [TH]  "รายงานเชิงเทคนิคของ DeepSeek-V3" (xyznot.com/th/paper/2412.19437),
+ *         Method §2 (equations for h'_t, s_{i,t}, g'_{i,t}; bias update) and
+ *         Key ideas, FP8 bullet (E4M3, 1x128 / 128x128 scaling, FP32
+ *         promotion every N_c = 128).
+ *   [YLY] "官方揭秘DeepSeek-V3模型训练全流程" (youleyou.com), §2.2
+ *         (no token dropping) and §4.3 FP8 训练.
+ *   [DB]  "Deepseek V3 国货之光 开源之光" (databean.com.cn), section
+ *         "Auxiliary-Loss-Free Load Balancing".
+ *
+ * Conventions shared by every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates device memory, never frees, and keeps no pointer after
+ *     a call returns.  Scratch comes from a caller-provided workspace.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work; they do not synchronise, except
+ *     moe_check_device_status, which says so.
+ *   - Types: bf16 = uint16_t bit pattern of bfloat16; fp8 = uint8_t code of
+ *     OCP FP8 E4M3FN (max 448, no infinities).  Layouts are row-major.
+ *   - Every call returns an int status (enum moe_status).  Arguments are
+ *     validated on the host before anything is enqueued; on a non-zero
+ *     status nothing was enqueued, except MOE_ERR_CUDA, which reports a
+ *     failed launch (moe_last_cuda_error() gives the cudaError_t of the
+ *     calling thread).  No call aborts or throws.
+ *   - Activation scales are stored "MN-major": scale of row r and K-block kb
+ *     at scales[kb * scale_ld + r].  Weight scales are per 128x128 block:
+ *     for a [G, N, K] weight stack, scale of group g, row block nb, column
+ *     block kb at scales[(g * (N/128) + nb) * (K/128) + kb].
+ */
+#ifndef MOE_FP8_H
+#define MOE_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,       /* null pointer, K > E, K > 32, E > 1024, negative size, ... */
+    MOE_ERR_UNSUPPORTED_SHAPE = -2, /* d or I not a multiple of 128, too many groups, ...        */
+    MOE_ERR_MISALIGNED = -3,        /* a pointer is not 16-byte aligned                           */
+    MOE_ERR_CUDA = -4,              /* a CUDA call failed; see moe_last_cuda_error()              */
+    MOE_ERR_TIMEOUT = -5,           /* a GEMM pipeline wait ran out (device status word)          */
+    MOE_ERR_WORKSPACE = -6,         /* workspace too small                                        */
+    MOE_ERR_BAD_INDEX = -7          /* device data held an index out of range (device status)     */
+};
+
+/* Grouped GEMM modes (moe_grouped_gemm_fp8). */
+enum moe_gemm_mode {
+    MOE_GEMM_GATE_UP_SILU_QUANT = 1, /* h = SiLU(A W_gate^T) * (A W_up^T), re-quantised 1x128 */
+    MOE_GEMM_DOWN = 2                /* y = A W_down^T, stored as bf16                         */
+};
+
+/* One DeepSeekMoE layer: d hidden, E routed experts (top-K of them per
+ * token), S shared experts, expert intermediate size I.  Weight stacks hold
+ * the E routed experts first and the S shared experts after them. */
+typedef struct moe_layer_t {
+    int d, E, K, S, I;
+    const float* centroids;   /* [E, d] expert centroids e_i                          */
+    const float* bias;        /* [E] selection bias b_i (moe_update_bias changes it)  */
+    const uint8_t* w_gate;    /* [E+S, I, d] fp8                                      */
+    const uint8_t* w_up;      /* [E+S, I, d] fp8                                      */
+    const uint8_t* w_down;    /* [E+S, d, I] fp8                                      */
+    const float* s_gate;      /* [E+S, I/128, d/128] block scales                     */
+    const float* s_up;        /* [E+S, I/128, d/128]                                  */
+    const float* s_down;      /* [E+S, d/128, I/128]                                  */
+} moe_layer_t;
+
+/* Text of a status code (static storage; never NULL). */
+const char* moe_status_string(int status);
+
+/* cudaError_t of the last failed CUDA call made by the calling thread. */
+int moe_last_cuda_error(void);
+
+/* Number of kernels this process has launched through the library. */
+uint64_t moe_kernel_launches(void);
+
+/* Workspace bytes moe_forward needs for up to T_max tokens of layer L
+ * (0 if L is invalid).  The same workspace serves moe_route and
+ * moe_permute at the same T. */
+size_t moe_workspace_size(const moe_layer_t* L, int T_max);
+
+/* Online 1x128 activation quantisation ([TH] Key ideas, FP8 bullet;
+ * [YLY] §4.3: online max-abs per 1x128 tile).  Output row r takes input row
+ * gather_rows[r] (or r when gather_rows is NULL; rows whose index is outside
+ * [0, n_src) are skipped and flagged MOE_ERR_BAD_INDEX in *status when status
+ * is not NULL).  Per tile: amax = max |x|; scale = amax / 448 (IEEE float32
+ * division); q = E4M3(x / scale) rounded to nearest even and saturated; a
+ * tile with amax = 0 gets scale 1 and all codes 0.
+ *   x [n_src, d] bf16;  q [M, d] fp8;  scales at scales[kb * scale_ld + r],
+ *   scale_ld >= M.  d must be a multiple of 128; x, q 16-byte aligned. */
+int moe_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather_rows, int M, int d,
+                    uint8_t* q, float* scales, int scale_ld, int32_t* status, void* stream);
+
+/* 128x128 block quantisation of a weight matrix ([TH] Key ideas, FP8 bullet;
+ * [YLY] §4.3), same rounding rule as moe_quant_1x128 with one scale per
+ * block.  w [R, C] float32; q [R, C] fp8; scales [R/128, C/128].  R and C
+ * multiples of 128; w and q 16-byte aligned. */
+int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, void* stream);
+
+/* Router ([TH] Method §2: s_{i,t} = Sigmoid(u_t^T e_i); g'_{i,t} = s_{i,t}
+ * when s_{i,t} + b_i is among the top K of {s_{j,t} + b_j}; g normalises g'.
+ * [DB]: the bias steers the selection only).  For every token t:
+ *   topk_idx [T, K] int32  experts by descending s + b (equal: lower index),
+ *   topk_gate [T, K] float s of each selected expert over their sum,
+ *   tie_flag [T] uint8     1 when the K-th and (K+1)-th biased scores differ
+ *                          by less than 1e-6 (their order may depend on
+ *                          rounding), else 0,
+ *   counts [E] int32       selections per expert (overwritten).
+ * u [T, d] bf16; centroids [E, d]; bias [E].  1 <= K <= min(E, 32),
+ * E <= 1024.  Workspace: at least T * E * 4 bytes, 256-byte aligned. */
+int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
+              int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch layout ([YLY] §2.2: no token is dropped, so every (token, slot)
+ * pair gets a row).  A stable counting sort of the T*K pairs by expert:
+ *   offsets [E+1]          exclusive scan of the per-expert counts,
+ *   perm_token [T*K]       token of each row (rows of one expert ascend by token),
+ *   inv_row [T, K]         row of each (token, slot).
+ * An expert index outside [0, E) is skipped and flagged MOE_ERR_BAD_INDEX in
+ * *status (if not NULL).  Workspace: moe_workspace_size of a layer with the
+ * same E and T (or at least 2 * ceil(T/64) * E * 4 + 4096 bytes). */
+int moe_permute(const int32_t* topk_idx, int T, int K, int E, int32_t* offsets,
+                int32_t* perm_token, int32_t* inv_row, int32_t* status, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* Grouped block-scaled FP8 GEMM on tcgen05 tensor cores ([TH] Key ideas,
+ * FP8 bullet; [YLY] §4.3: each 128-wide K slab is summed on the tensor core
+ * and promoted to an FP32 accumulator with its 1x128 activation scale and
+ * 128x128 weight scale: acc += partial * (sa * sw)).
+ *   A [M_total, Kdim] fp8, sa [Kdim/128][M_total];
+ *   group_offsets [G+1] (device): group g owns rows [go[g], go[g+1]) of A
+ *   and of the output, and uses weight slice g.
+ *   W0 [G, N, Kdim] fp8, sw0 [G, N/128, Kdim/128]; W1 / sw1 the same shape
+ *   (GATE_UP mode only, NULL for DOWN).
+ *   mode GATE_UP_SILU_QUANT: W0 = W_gate, W1 = W_up, N = I; out = h codes
+ *     [M_total, N] fp8 with out_scales [N/128][M_total], where
+ *     h = SiLU(A W0^T) * (A W1^T), SiLU(x) = x / (1 + exp(-x)), quantised
+ *     per 1x128 tile with the moe_quant_1x128 rule.
+ *   mode DOWN: W0 = W_down, N = d; out = y [M_total, N] bf16 (round to
+ *     nearest even); out_scales unused.
+ * Rows outside every group are left untouched.  Kdim and N multiples of 128;
+ * G <= 1088; all pointers 16-byte aligned.  status (device int32, nullable)
+ * receives MOE_ERR_TIMEOUT if a pipeline wait ran out (the kernel then stops
+ * early and its output is incomplete). */
+int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_total,
+                         const int32_t* group_offsets, int G, const uint8_t* W0,
+                         const uint8_t* W1, const float* sw0, const float* sw1, int N, int Kdim,
+                         void* out, float* out_scales, int32_t* status, void* stream);
+
+/* Combine ([TH] Method §2: h'_t = u_t + sum_s FFN_s(u_t) + sum_i g_{i,t}
+ * FFN_i(u_t)).  h_out[t] = u[t] + sum_s Y_shared[s*T + t] +
+ * sum_k topk_gate[t,k] * Y[inv_row[t,k]], summed in float32.
+ *   u [T, d] bf16; Y [*, d] bf16 (routed rows); Y_shared [S*T, d] bf16
+ *   (may be NULL when S = 0); h_out [T, d] float32.  d multiple of 8;
+ *   pointers 16-byte aligned. */
+int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
+                const int32_t* inv_row, const uint16_t* Y_shared, int T, int d, int K, int S,
+                float* h_out, void* stream);
+
+/* The whole layer forward: route, dispatch, quantise, GEMM (gate/up + SiLU),
+ * GEMM (down), combine -- all enqueued on `stream` with no host sync.
+ * Outputs: h_out [T, d] float32 and the routing (topk_idx, topk_gate,
+ * counts, tie_flag as in moe_route), which moe_update_bias consumes.
+ * ws: at least moe_workspace_size(L, T) bytes, 256-byte aligned.  Its first
+ * 16 bytes hold the device status word of this call (read it with
+ * moe_check_device_status(ws, stream)). */
+int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
+                float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* Auxiliary-loss-free bias update at the end of a step ([TH] Method §2:
+ * b_i -= gamma when expert i is overloaded, += gamma when underloaded;
+ * gamma = 0.001 there).  With n = T*K selections, expert e is overloaded when
+ * counts[e] * E > n and underloaded when counts[e] * E < n; equal load keeps
+ * b_e.  bias [E] float32 is updated in place. */
+int moe_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,
+                    void* stream);
+
+/* Waits for `stream`, reads the device status word at `status` (written by
+ * moe_quant_1x128, moe_permute, moe_grouped_gemm_fp8 or moe_forward) and
+ * returns it (MOE_OK when nothing was flagged), then clears it. */
+int moe_check_device_status(int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP8_H */

@@ -217,16 +217,15 @@ void orc_gemm_fp8(const uint8_t* qa, const float* sa, int M, int Kd,
         }
 }
 
-/* One expert FFN on quantised activation rows (R7, R8).
+/* Gate/up half of one expert FFN (R7, R8): h = SiLU(A Wg^T) * (A Wu^T),
+ * quantised per 1x128 tile along I.
  *   qa [M, d], sa [M, d/128]; wg, wu [I, d] with sg, su [I/128, d/128];
- *   wd [d, I] with sd [d/128, I/128]; y [M, d] float32.                    */
-void orc_expert_ffn(const uint8_t* qa, const float* sa, int M, int d, int I,
-                    const uint8_t* wg, const float* sg, const uint8_t* wu, const float* su,
-                    const uint8_t* wd, const float* sd, float* y) {
+ *   outputs qh [M, I] codes and sh [M, I/128] scales.                      */
+void orc_gate_up(const uint8_t* qa, const float* sa, int M, int d, int I,
+                 const uint8_t* wg, const float* sg, const uint8_t* wu, const float* su,
+                 uint8_t* qh, float* sh) {
     float* G = (float*)malloc(sizeof(float) * (size_t)M * I);
     float* U = (float*)malloc(sizeof(float) * (size_t)M * I);
-    uint8_t* qh = (uint8_t*)malloc((size_t)M * I);
-    float* sh = (float*)malloc(sizeof(float) * (size_t)M * (I / 128));
     orc_gemm_fp8(qa, sa, M, d, wg, sg, I, G);
     orc_gemm_fp8(qa, sa, M, d, wu, su, I, U);
     for (int64_t i = 0; i < (int64_t)M * I; ++i) {
@@ -235,8 +234,20 @@ void orc_expert_ffn(const uint8_t* qa, const float* sa, int M, int d, int I,
         G[i] = silu * U[i]; /* G now holds h */
     }
     orc_quant_1x128_f32(G, M, I, qh, sh);
+    free(G); free(U);
+}
+
+/* One expert FFN on quantised activation rows: the gate/up half, then the
+ * down projection of the quantised h (R7, R8).
+ *   wd [d, I] with sd [d/128, I/128]; y [M, d] float32.                    */
+void orc_expert_ffn(const uint8_t* qa, const float* sa, int M, int d, int I,
+                    const uint8_t* wg, const float* sg, const uint8_t* wu, const float* su,
+                    const uint8_t* wd, const float* sd, float* y) {
+    uint8_t* qh = (uint8_t*)malloc((size_t)M * I);
+    float* sh = (float*)malloc(sizeof(float) * (size_t)M * (I / 128));
+    orc_gate_up(qa, sa, M, d, I, wg, sg, wu, su, qh, sh);
     orc_gemm_fp8(qh, sh, M, I, wd, sd, d, y);
-    free(G); free(U); free(qh); free(sh);
+    free(qh); free(sh);
 }
 
 /* ------------------------------------------------------------------ */

@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
         _lib.orc_quant_128x128.argtypes = [P, i32, i32, P, P]
         _lib.orc_gemm_fp8.argtypes = [P, P, i32, i32, P, P, i32, P]
         _lib.orc_expert_ffn.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P]
+        _lib.orc_gate_up.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P]
         _lib.orc_route.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P]
         _lib.orc_dispatch.restype = i32
         _lib.orc_dispatch.argtypes = [P, i32, i32, i32, P, P, P, P]
@@ -117,6 +118,18 @@ def gemm_fp8(qa, sa, qw, sw) -> np.ndarray:
     out = np.empty((M, N), np.float32)
     lib().orc_gemm_fp8(_p(qa), _p(sa), M, K, _p(qw), _p(sw), N, _p(out))
     return out
+
+
+def gate_up(qa, sa, wg, sg, wu, su) -> tuple[np.ndarray, np.ndarray]:
+    """h = SiLU(A Wg^T) * (A Wu^T) quantised 1x128 -> (codes [M, I], scales [M, I/128])."""
+    qa, sa = _c(qa, np.uint8), _c(sa, np.float32)
+    wg, wu, sg, su = _c(wg, np.uint8), _c(wu, np.uint8), _c(sg, np.float32), _c(su, np.float32)
+    M, d = qa.shape
+    I = wg.shape[0]
+    qh = np.empty((M, I), np.uint8)
+    sh = np.empty((M, I // 128), np.float32)
+    lib().orc_gate_up(_p(qa), _p(sa), M, d, I, _p(wg), _p(sg), _p(wu), _p(su), _p(qh), _p(sh))
+    return qh, sh
 
 
 def expert_ffn(qa, sa, wg, sg, wu, su, wd, sd) -> np.ndarray:

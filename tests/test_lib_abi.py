@@ -1,0 +1,92 @@
+"""The C ABI library loads without a GPU, exports every declared entry point,
+and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fine_grained_fp8_bias_b300 import build
+    build.build()
+    from fine_grained_fp8_bias_b300 import lib as L
+    return L
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 13
+    for n in ("moe_route", "moe_permute", "moe_quant_1x128", "moe_grouped_gemm_fp8",
+              "moe_combine", "moe_forward", "moe_update_bias", "moe_workspace_size",
+              "moe_status_string"):
+        assert n in names
+    for n in names:
+        assert hasattr(lib.lib(), n), n
+
+
+def test_status_strings(lib):
+    L = lib.lib()
+    assert L.moe_status_string(0) == b"ok"
+    for code in range(-7, 0):
+        assert L.moe_status_string(code) not in (b"", b"unknown status")
+
+
+def test_host_side_validation_needs_no_device(lib):
+    L = lib.lib()
+    fake = 1 << 20                     # never dereferenced: every call below fails validation
+    # d not a multiple of 128
+    assert L.moe_quant_1x128(fake, 4, None, 4, 100, fake, fake, 4, None, None) == -2
+    assert L.moe_quant_128x128(fake, 100, 128, fake, fake, None) == -2
+    # K > E, K > 32, E > 1024
+    assert L.moe_route(fake, fake, fake, 4, 128, 4, 5, fake, fake, fake, fake, fake, 1 << 20, None) == -1
+    assert L.moe_route(fake, fake, fake, 4, 128, 64, 33, fake, fake, fake, fake, fake, 1 << 20, None) == -1
+    assert L.moe_route(fake, fake, fake, 4, 128, 2048, 8, fake, fake, fake, fake, fake, 1 << 20, None) == -1
+    # workspace too small, misaligned pointer
+    assert L.moe_route(fake, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 16, None) == -6
+    assert L.moe_route(fake + 8, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 1 << 20, None) == -3
+    assert L.moe_permute(fake, 4, 2, 8, fake, fake, fake, None, fake, 0, None) == -6
+    # GEMM: bad mode, N not a multiple of 128, too many groups, null pointers
+    assert L.moe_grouped_gemm_fp8(3, fake, fake, 8, fake, 1, fake, None, fake, None, 128, 128,
+                                  fake, None, None, None) == -1
+    assert L.moe_grouped_gemm_fp8(2, fake, fake, 8, fake, 1, fake, None, fake, None, 100, 128,
+                                  fake, None, None, None) == -2
+    assert L.moe_grouped_gemm_fp8(2, fake, fake, 8, fake, 5000, fake, None, fake, None, 128, 128,
+                                  fake, None, None, None) == -2
+    assert L.moe_grouped_gemm_fp8(1, fake, fake, 8, fake, 1, fake, None, fake, None, 128, 128,
+                                  fake, None, None, None) == -1
+    assert L.moe_combine(fake, fake, fake, fake, fake, 4, 100, 2, 1, fake, None) == -2
+    assert L.moe_update_bias(None, 8, 4, 2, ctypes.c_float(1e-3), fake, None) == -1
+    assert L.moe_forward(None, fake, 4, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -1
+
+
+def test_workspace_size_and_layer_checks(lib):
+    L = lib.lib()
+    layer = lib.moe_layer_t(7168, 256, 8, 1, 2048, *([1 << 20] * 8))
+    n = L.moe_workspace_size(ctypes.byref(layer), 4096)
+    M = 4096 * 9
+    # the routed + shared activation copies, h and y dominate
+    assert n >= M * 7168 + M * 2048 + 2 * M * 7168
+    assert L.moe_workspace_size(ctypes.byref(layer), 0) > 0
+    bad = lib.moe_layer_t(7000, 256, 8, 1, 2048, *([1 << 20] * 8))
+    assert L.moe_forward(ctypes.byref(bad), 1 << 20, 4, 1 << 20, 1 << 20, 1 << 20, 1 << 20,
+                         1 << 20, 1 << 20, 1 << 40, None) == -2
+    k_too_big = lib.moe_layer_t(7168, 4, 8, 1, 2048, *([1 << 20] * 8))
+    assert L.moe_forward(ctypes.byref(k_too_big), 1 << 20, 4, 1 << 20, 1 << 20, 1 << 20,
+                         1 << 20, 1 << 20, 1 << 20, 1 << 40, None) == -1
+    # workspace smaller than required
+    assert L.moe_forward(ctypes.byref(layer), 1 << 20, 4096, 1 << 20, 1 << 20, 1 << 20, 1 << 20,
+                         1 << 20, 1 << 20, 1024, None) == -6
