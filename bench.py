@@ -1,0 +1,466 @@
+"""Benchmark of the DeepSeekMoE FP8 layer forward + bias update on B300.
+
+One step = the whole path over one batch: route (logits, sigmoid, biased
+top-K, gates, counts) -> dispatch -> 1x128 quantisation of the gathered
+activations -> grouped FP8 GEMM gate/up + SiLU + re-quantisation -> grouped
+FP8 GEMM down -> combine with shared expert and residual -> bias update.
+Every step runs in libmoefp8's kernels, called through its C ABI.
+
+Default workload: the V3-shape prefill batch (T=4096 tokens, d=7168, 256
+routed experts top-8 + 1 shared, intermediate 2048), synthetic seeded data
+and weights.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C implementation used as
+the correctness reference) on the host cores, on a bounded sample of the
+same workload.  With N > 1 (torchrun) every rank runs an independent replica
+of the layer on its own GPU (the path has no cross-GPU exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fine_grained_fp8_bias_b300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at d=7168,256e top-8; FP8 GEMM % peak; decode HBM GB/s"
+FP8_OVER_BF16 = 2.0   # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
+STAGES = ["route", "permute", "quant", "gemm_gate_up", "gemm_down", "combine", "bias_update"]
+KERNELS_PER_STAGE = {"route": 2, "permute": 3, "quant": 1, "gemm_gate_up": 1, "gemm_down": 1,
+                     "combine": 1, "bias_update": 1}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit())}
+
+
+# ----------------------------------------------------------- GPU path
+class Step:
+    """Buffers and the component calls of one step (the same sequence moe_forward runs)."""
+
+    def __init__(self, layer, u, gamma):
+        from fine_grained_fp8_bias_b300 import lib
+        self.lib = lib
+        self.L = layer
+        self.u = u
+        self.gamma = gamma
+        T, d, E, K, S, I = u.shape[0], layer.d, layer.E, layer.K, layer.S, layer.I
+        self.T, self.M = T, T * (K + S)
+        dev = u.device
+        M = self.M
+        self.route_ws = torch.empty(max(4 * T * E, 256), dtype=torch.uint8, device=dev)
+        nchunks = (T + 63) // 64
+        self.perm_ws = torch.empty(2 * ((4 * nchunks * E + 255) // 256 * 256) + 256,
+                                   dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.rout = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),
+                     "gate": torch.empty((T, K), dtype=torch.float32, device=dev),
+                     "tie": torch.empty((T,), dtype=torch.uint8, device=dev),
+                     "counts": torch.empty((E,), dtype=torch.int32, device=dev)}
+        self.pout = {"offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
+                     "group_offsets": torch.empty((E + S + 1,), dtype=torch.int32, device=dev),
+                     "perm_token": torch.empty((M,), dtype=torch.int32, device=dev),
+                     "inv_row": torch.empty((T, K), dtype=torch.int32, device=dev)}
+        self.A = torch.empty((M, d), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((d // 128, M), dtype=torch.float32, device=dev)
+        self.H = torch.empty((M, I), dtype=torch.uint8, device=dev)
+        self.sh = torch.empty((I // 128, M), dtype=torch.float32, device=dev)
+        self.Y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+        self.h = torch.empty((T, d), dtype=torch.float32, device=dev)
+
+    def stage(self, name):
+        lib, L = self.lib, self.L
+        if name == "route":
+            lib.moe_route(self.u, L.centroids, L.bias, L.K, ws=self.route_ws, out=self.rout)
+        elif name == "permute":
+            lib.moe_permute(self.rout["idx"], L.E, L.S, ws=self.perm_ws, status=self.status,
+                            out=self.pout)
+        elif name == "quant":
+            lib.moe_quant_1x128(self.u, self.pout["perm_token"], M=self.M, q=self.A,
+                                scales=self.sa, status=self.status)
+        elif name == "gemm_gate_up":
+            lib.moe_grouped_gemm_fp8(lib.MOE_GEMM_GATE_UP_SILU_QUANT, self.A, self.sa,
+                                     self.pout["group_offsets"], L.w_gate, L.w_up, L.s_gate,
+                                     L.s_up, out=self.H, out_scales=self.sh, status=self.status)
+        elif name == "gemm_down":
+            lib.moe_grouped_gemm_fp8(lib.MOE_GEMM_DOWN, self.H, self.sh,
+                                     self.pout["group_offsets"], L.w_down, None, L.s_down, None,
+                                     out=self.Y, status=self.status)
+        elif name == "combine":
+            TK = self.T * L.K
+            lib.moe_combine(self.u, self.Y, self.rout["gate"], self.pout["inv_row"],
+                            self.Y[TK:] if L.S else None, L.S, h=self.h)
+        elif name == "bias_update":
+            lib.moe_update_bias(self.rout["counts"], L.bias, self.T, L.K, self.gamma)
+
+    def run(self, events=None):
+        for i, name in enumerate(STAGES):
+            self.stage(name)
+            if events is not None:
+                events[i].record()
+
+
+def algorithmic_bytes(cfg, T, touched: int) -> dict:
+    """Minimal HBM bytes of each stage (each input read once, each output written once)."""
+    d, E, K, S, I = cfg.d, cfg.E, cfg.K, cfg.S, cfg.I
+    M = T * (K + S)
+    wsc = lambda n, k: (n // 128) * (k // 128) * 4
+    return {
+        "route": T * d * 2 + E * d * 4 + E * 4 + T * K * 8 + T + E * 4,
+        "permute": T * K * 4 + M * 4 + T * K * 4 + (E + S + 1) * 4 * 2,
+        "quant": T * d * 2 + M * 4 + M * d + M * (d // 128) * 4,
+        "gemm_gate_up": touched * 2 * (I * d + wsc(I, d)) + M * d + M * (d // 128) * 4
+        + M * I + M * (I // 128) * 4,
+        "gemm_down": touched * (d * I + wsc(d, I)) + M * I + M * (I // 128) * 4 + M * d * 2,
+        "combine": T * d * 2 + M * d * 2 + T * K * 8 + T * d * 4,
+        "bias_update": E * 4 * 3,
+    }
+
+
+def gemm_flops(cfg, T) -> dict:
+    M = T * (cfg.K + cfg.S)
+    return {"gemm_gate_up": 2.0 * M * 2 * cfg.I * cfg.d, "gemm_down": 2.0 * M * cfg.d * cfg.I}
+
+
+def kernel_traffic(stage: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, "fine_grained_fp8_bias_b300", "csrc", d.get("source_file", ""))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    e = d.get("kernels", {}).get(stage)
+    if e is None or d.get("source_sha256_16") != h:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_ours(args, world, rank, local):
+    from fine_grained_fp8_bias_b300 import lib
+    from fine_grained_fp8_bias_b300.layer import MoELayer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = wl.CONFIGS[args.workload]
+    pk = peaks()
+    layer = MoELayer.from_config(cfg, dev)
+    u = wl.tokens(cfg, dev)
+    step = Step(layer, u, cfg.gamma)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if lib.moe_check_device_status(step.status) != 0:
+        raise RuntimeError("device status flagged during warm-up")
+
+    n_ev = len(STAGES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = lib.kernel_launches()
+    start.record(stream)
+    per_stage = {s: 0.0 for s in STAGES}
+    for k in range(args.steps):
+        step.run(evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    launches = lib.kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    for k in range(args.steps):
+        for i, s in enumerate(STAGES):
+            a = start if (k == 0 and i == 0) else (evs[k][i - 1] if i > 0 else evs[k - 1][-1])
+            per_stage[s] += a.elapsed_time(evs[k][i])
+    if lib.moe_check_device_status(step.status) != 0:
+        raise RuntimeError("device status flagged during the timed region")
+
+    counts = step.rout["counts"].cpu()
+    touched = int((counts > 0).sum()) + cfg.S
+    T = cfg.T
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # per-kernel roofline
+    abytes = algorithmic_bytes(cfg, T, touched)
+    flops = gemm_flops(cfg, T)
+    kernels = {}
+    for s in STAGES:
+        ms = per_stage[s] / args.steps
+        kernels[s] = {"ms": round(ms, 4), "share": round(per_stage[s] / sum(per_stage.values()), 4),
+                      "GBps": round(abytes[s] / (ms * 1e-3) / 1e9, 1)}
+        if s in flops:
+            kernels[s]["TFLOPs"] = round(flops[s] / (ms * 1e-3) / 1e12, 1)
+    dom = max(STAGES, key=lambda s: per_stage[s])
+    dom_ms = per_stage[dom] / args.steps
+    achieved = abytes[dom] / (dom_ms * 1e-3) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": kernel_traffic(dom), "algorithmic_bytes": abytes[dom],
+                "peak_source": f"{pk['source']} HBM copy bandwidth"}
+    fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    fp8 = {s: {"TFLOPs": kernels[s]["TFLOPs"], "frac_of_fp8_peak": round(
+        kernels[s]["TFLOPs"] / fp8_peak, 4)} for s in flops}
+    fp8["peak_TFLOPs"] = fp8_peak
+    fp8["peak_source"] = f"{pk['source']} bf16 burst x nominal FP8/BF16 ratio 2"
+
+    e2e = run_e2e(layer, cfg, dev, max(3, min(args.steps, 30)), world)
+    decode = run_decode(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded counter-based generator; random-init weights quantised 128x128)",
+        "config": {**wl.describe(cfg), "inputs": "resident in HBM; weights 11.3 GB > L2, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline, "fp8_gemm": fp8, "kernels": kernels,
+        "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+    }
+    if decode:
+        line["decode"] = decode
+    return line
+
+
+def run_e2e(layer, cfg, dev, steps, world):
+    """Whole-job throughput through moe_forward with host buffers: H2D copy of u
+    from pinned memory, forward, bias update and D2H copy of h' every step."""
+    u_host = wl.pinned_like(wl.tokens(cfg, "cpu"))
+    h_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32, pin_memory=True)
+    u_dev = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+    out = layer.outputs(cfg.T)
+    for _ in range(2):
+        u_dev.copy_(u_host, non_blocking=True)
+        layer.forward(u_dev, out)
+        layer.update_bias(out["counts"], cfg.T, cfg.gamma)
+        h_host.copy_(out["h"], non_blocking=True)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    s.record()
+    for _ in range(steps):
+        u_dev.copy_(u_host, non_blocking=True)
+        layer.forward(u_dev, out)
+        layer.update_bias(out["counts"], cfg.T, cfg.gamma)
+        h_host.copy_(out["h"], non_blocking=True)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if layer.status() != 0:
+        raise RuntimeError("device status flagged in the end-to-end loop")
+    return {"value": round(world * cfg.T * steps / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 4,
+            "steps": steps, "ms_per_step": round(ms / steps, 4)}
+
+
+def run_decode(layer, cfg, dev, pk, T=64, steps=50):
+    """Decode-sized batch on the same V3 weights: forward time and the HBM rate of
+    the weights it touches (distinct experts + shared)."""
+    dcfg = wl.V3_DECODE.with_(T=T)
+    u = wl.tokens(dcfg, dev)
+    out = layer.outputs(T)
+    for _ in range(5):
+        layer.forward(u, out)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        layer.forward(u, out)
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) / steps * 1e3
+    touched = int((out["counts"].cpu() > 0).sum()) + cfg.S
+    wbytes = touched * 3 * cfg.d * cfg.I * (1 + 4 / 128 ** 2)
+    return {"T": T, "us_per_forward": round(us, 1), "experts_touched": touched,
+            "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
+            "frac_of_hbm": round(wbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4)}
+
+
+# ------------------------------------------------------ CPU oracle arm
+def oracle_setup(cfg, n_tok):
+    from oracle import oracle as orc
+    orc.build()
+    u = wl.tokens(cfg, "cpu")[:n_tok]
+    ub = u.view(torch.int16).numpy().view("uint16")
+    cent = wl.centroids(cfg).numpy()
+    b = wl.bias(cfg).numpy()
+    r = orc.route(ub, cent, b, cfg.K)
+    groups = set(range(cfg.E, cfg.E + cfg.S)) | {int(e) for e in r["idx"].ravel()}
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = orc.quantised_weights(cfg, sorted(groups),
+                              lambda which, g: wl.master_weight(cfg, which, g, gen_dev).cpu().numpy())
+    return orc, ub, cent, b, W
+
+
+def oracle_step(orc, cfg, ub, cent, b, W, toks):
+    r = orc.route(ub[toks], cent, b, cfg.K)
+    orc.layer_forward(ub[toks], r["idx"], r["gate"], W, cfg.d, cfg.E, cfg.K, cfg.S, cfg.I,
+                      list(range(len(toks))))
+    orc.update_bias(r["counts"], b, len(toks), cfg.K, cfg.gamma)
+
+
+def cpu_baseline(cfg, n_tok=2, reps=2):
+    orc, ub, cent, b, W = oracle_setup(cfg, n_tok)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(orc, cfg, ub, cent, b, W, list(range(n_tok)))
+    dt = time.perf_counter() - t0
+    return {"value": round(reps * n_tok / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_tok} tokens of the {cfg.name} batch, {reps} passes: routing over all "
+                      f"{cfg.E} experts, 1x128 quantisation, {cfg.K} routed + {cfg.S} shared "
+                      f"expert FFNs per token, combine, bias update (single thread)"}
+
+
+def run_reference(args):
+    cfg = wl.CONFIGS[args.workload]
+    n_tok = 2
+    orc, ub, cent, b, W = oracle_setup(cfg, n_tok)
+    for k in range(args.warmup):
+        oracle_step(orc, cfg, ub, cent, b, W, [k % n_tok])
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        oracle_step(orc, cfg, ub, cent, b, W, [k % n_tok])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (E4M3 emulated)",
+            "data": "synthetic", "config": wl.describe(cfg),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"each step one token of the {cfg.name} batch (cycling over "
+                                       f"its first {n_tok}): routing, quantisation, {cfg.K}+{cfg.S} "
+                                       f"expert FFNs, combine, bias update"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="v3_prefill", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl.CONFIGS[args.workload])
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

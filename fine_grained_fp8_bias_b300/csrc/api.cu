@@ -34,7 +34,7 @@ Layout layout(int T, int d, int E, int K, int S, int I) {
     L.base = take(sizeof(int32_t) * nchunks * E);
     L.go = take(sizeof(int32_t) * (size_t)(E + S + 1));
     L.offsets = take(sizeof(int32_t) * (size_t)(E + 1));
-    L.perm = take(sizeof(int32_t) * (size_t)T * K);
+    L.perm = take(sizeof(int32_t) * M);
     L.inv_row = take(sizeof(int32_t) * (size_t)T * K);
     L.A = take(M * d);
     L.sa = take(sizeof(float) * M * (d / 128));
@@ -112,8 +112,9 @@ int moe_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather_rows, in
     if (M == 0) return MOE_OK;
     if (!x || !q || !scales) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q)) return MOE_ERR_MISALIGNED;
-    return launch_quant_1x128(x, n_src, gather_rows, M, M, 1, d, q, scales, scale_ld, status,
-                              S_(stream));
+    // every output row is a gathered row (no shared-expert tail)
+    return launch_quant_1x128(x, n_src, gather_rows, /*n_gather=*/M, /*tail_T=*/1, M, d, q, scales,
+                              scale_ld, status, S_(stream));
 }
 
 int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, void* stream) {
@@ -139,11 +140,12 @@ int moe_route(const uint16_t* u, const float* centroids, const float* bias, int 
                         static_cast<float*>(ws), S_(stream));
 }
 
-int moe_permute(const int32_t* topk_idx, int T, int K, int E, int32_t* offsets,
-                int32_t* perm_token, int32_t* inv_row, int32_t* status, void* ws,
-                size_t ws_bytes, void* stream) {
-    if (T < 0 || K <= 0 || E <= 0 || K > E || K > kMaxTopK || E > kMaxExperts)
+int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* offsets,
+                int32_t* group_offsets, int32_t* perm_token, int32_t* inv_row, int32_t* status,
+                void* ws, size_t ws_bytes, void* stream) {
+    if (T < 0 || K <= 0 || E <= 0 || S < 0 || K > E || K > kMaxTopK || E > kMaxExperts)
         return MOE_ERR_INVALID_ARG;
+    if ((long long)T * (K + S) > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!offsets || !ws || (T > 0 && (!topk_idx || !perm_token || !inv_row)))
         return MOE_ERR_INVALID_ARG;
     const size_t nchunks = ((size_t)T + kPermuteChunk - 1) / kPermuteChunk;
@@ -152,8 +154,8 @@ int moe_permute(const int32_t* topk_idx, int T, int K, int E, int32_t* offsets,
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
     int32_t* hist = static_cast<int32_t*>(ws);
     int32_t* base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + hist_bytes);
-    return launch_permute(topk_idx, T, K, E, offsets, perm_token, inv_row, nullptr, 0, status,
-                          hist, base, S_(stream));
+    return launch_permute(topk_idx, T, K, E, offsets, perm_token, inv_row, group_offsets, S,
+                          status, hist, base, S_(stream));
 }
 
 int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_total,
@@ -194,6 +196,7 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     int rc = check_layer(L);
     if (rc) return rc;
     if (T < 0) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * (L->K + L->S) > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!ws || !counts) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!u || !h_out || !topk_idx || !topk_gate || !tie_flag)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(u) || !aligned16(h_out)) return MOE_ERR_MISALIGNED;
@@ -209,7 +212,7 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     int32_t* bbase = reinterpret_cast<int32_t*>(base + W.base);
     int32_t* go = reinterpret_cast<int32_t*>(base + W.go);
     int32_t* offsets = reinterpret_cast<int32_t*>(base + W.offsets);
-    int32_t* perm = reinterpret_cast<int32_t*>(base + W.perm);
+    int32_t* perm = reinterpret_cast<int32_t*>(base + W.perm);   // T*(K+S) rows
     int32_t* inv_row = reinterpret_cast<int32_t*>(base + W.inv_row);
     uint8_t* A = reinterpret_cast<uint8_t*>(base + W.A);
     float* sa = reinterpret_cast<float*>(base + W.sa);
@@ -227,7 +230,7 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,
                              st)))
         return rc;
-    if ((rc = launch_quant_1x128(u, T, perm, T * K, T, M, d, A, sa, M, status, st))) return rc;
+    if ((rc = launch_quant_1x128(u, T, perm, M, 1, M, d, A, sa, M, status, st))) return rc;
     if ((rc = launch_grouped_gemm(MOE_GEMM_GATE_UP_SILU_QUANT, A, sa, M, go, G, L->w_gate,
                                   L->w_up, L->s_gate, L->s_up, I, d, H, sh, status, st)))
         return rc;

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
 
 // One block of 1024 threads.  base[b][e] = offsets[e] + sum_{b' < b} hist[b'][e].
 // Optionally writes the grouped-GEMM group offsets: E routed groups, then S
-// shared groups of T rows each after the T*K routed rows.
+// shared groups of T rows each after the T*K routed rows (E+S+1 entries).
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist, int nchunks,
                                                     int E, int T, int K, int S,
                                                     int32_t* __restrict__ base,
@@ -86,8 +86,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     }
 }
 
+// Also writes the rows of the S shared-expert groups: row T*K + s*T + t is
+// token t.
 __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ idx, int T,
-                                                      int K, int E,
+                                                      int K, int E, int S,
                                                       const int32_t* __restrict__ base,
                                                       int32_t* __restrict__ perm,
                                                       int32_t* __restrict__ inv_row) {
@@ -95,6 +97,10 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
     const int t0 = blockIdx.x * kPermuteChunk;
     const int t1 = min(T, t0 + kPermuteChunk);
     const int n = (t1 - t0) * K;
+    for (int p = threadIdx.x; p < S * (t1 - t0); p += blockDim.x) {
+        const int s = p / (t1 - t0), t = t0 + p % (t1 - t0);
+        perm[(size_t)T * K + (size_t)s * T + t] = t;
+    }
     for (int p = threadIdx.x; p < n; p += blockDim.x) sel[p] = idx[(size_t)t0 * K + p];
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -126,7 +132,7 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, in
     if (rc) return rc;
     if (nchunks > 0) {
         scatter_kernel<<<nchunks, 256, sizeof(int32_t) * kPermuteChunk * K, st>>>(
-            idx, T, K, E, ws_base, perm, inv_row);
+            idx, T, K, E, S, ws_base, perm, inv_row);
         rc = check_launch();
     }
     return rc;

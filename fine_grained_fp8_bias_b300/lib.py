@@ -54,7 +54,7 @@ def _load() -> ctypes.CDLL:
         "moe_quant_1x128": [P, I32, P, I32, I32, P, P, I32, P, P],
         "moe_quant_128x128": [P, I32, I32, P, P, P],
         "moe_route": [P, P, P, I32, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
-        "moe_permute": [P, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
+        "moe_permute": [P, I32, I32, I32, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_grouped_gemm_fp8": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
         "moe_combine": [P, P, P, P, P, I32, I32, I32, I32, P, P],
         "moe_forward": [ctypes.POINTER(moe_layer_t), P, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
@@ -165,19 +165,23 @@ def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: i
     return out
 
 
-def moe_permute(topk_idx: torch.Tensor, E: int, ws: Optional[torch.Tensor] = None,
-                status: Optional[torch.Tensor] = None, stream=None) -> dict:
+def moe_permute(topk_idx: torch.Tensor, E: int, S: int = 0, ws: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+                stream=None) -> dict:
     _dev(topk_idx, "topk_idx")
     T, K = topk_idx.shape
     dev = topk_idx.device
-    out = {"offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
-           "perm_token": torch.empty((T * K,), dtype=torch.int32, device=dev),
-           "inv_row": torch.empty((T, K), dtype=torch.int32, device=dev)}
+    if out is None:
+        out = {"offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
+               "group_offsets": torch.empty((E + S + 1,), dtype=torch.int32, device=dev),
+               "perm_token": torch.empty((T * (K + S),), dtype=torch.int32, device=dev),
+               "inv_row": torch.empty((T, K), dtype=torch.int32, device=dev)}
     if ws is None:
         nchunks = (T + 63) // 64
         ws = torch.empty(2 * ((4 * nchunks * E + 255) // 256 * 256) + 256, dtype=torch.uint8,
                          device=dev)
-    _check(_lib.moe_permute(_ptr(topk_idx), T, K, E, _ptr(out["offsets"]), _ptr(out["perm_token"]),
+    _check(_lib.moe_permute(_ptr(topk_idx), T, K, E, S, _ptr(out["offsets"]),
+                            _ptr(out.get("group_offsets")), _ptr(out["perm_token"]),
                             _ptr(out["inv_row"]), _ptr(status), _ptr(ws),
                             ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
     return out

@@ -122,16 +122,22 @@ int moe_route(const uint16_t* u, const float* centroids, const float* bias, int 
               void* ws, size_t ws_bytes, void* stream);
 
 /* Dispatch layout ([YLY] §2.2: no token is dropped, so every (token, slot)
- * pair gets a row).  A stable counting sort of the T*K pairs by expert:
+ * pair gets a row).  A stable counting sort of the T*K pairs by expert, plus
+ * the rows of the S shared experts, which see every token:
  *   offsets [E+1]          exclusive scan of the per-expert counts,
- *   perm_token [T*K]       token of each row (rows of one expert ascend by token),
- *   inv_row [T, K]         row of each (token, slot).
+ *   group_offsets [E+S+1]  (nullable) rows of the E routed groups followed by
+ *                          S shared groups of T rows each -- the
+ *                          group_offsets of moe_grouped_gemm_fp8,
+ *   perm_token [T*(K+S)]   token of each row: routed rows of one expert
+ *                          ascend by token; row T*K + s*T + t is token t,
+ *   inv_row [T, K]         routed row of each (token, slot).
  * An expert index outside [0, E) is skipped and flagged MOE_ERR_BAD_INDEX in
  * *status (if not NULL).  Workspace: moe_workspace_size of a layer with the
- * same E and T (or at least 2 * ceil(T/64) * E * 4 + 4096 bytes). */
-int moe_permute(const int32_t* topk_idx, int T, int K, int E, int32_t* offsets,
-                int32_t* perm_token, int32_t* inv_row, int32_t* status, void* ws,
-                size_t ws_bytes, void* stream);
+ * same E and T (or at least 2 * 256-byte-rounded ceil(T/64) * E * 4 bytes),
+ * 256-byte aligned. */
+int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* offsets,
+                int32_t* group_offsets, int32_t* perm_token, int32_t* inv_row, int32_t* status,
+                void* ws, size_t ws_bytes, void* stream);
 
 /* Grouped block-scaled FP8 GEMM on tcgen05 tensor cores ([TH] Key ideas,
  * FP8 bullet; [YLY] §4.3: each 128-wide K slab is summed on the tensor core

@@ -133,12 +133,18 @@ def test_permute_bit_exact(L, orc, T, K, E):
     rng = np.random.default_rng(T * 7 + E)
     pool = np.array([e for e in range(E) if e != 2 or E <= K + 1])   # expert 2 stays empty
     idx = np.stack([rng.choice(pool, K, replace=False) for _ in range(T)]).astype(np.int32)
-    out = L.moe_permute(torch.from_numpy(idx).cuda(), E)
+    S = 2
+    out = L.moe_permute(torch.from_numpy(idx).cuda(), E, S)
     torch.cuda.synchronize()
     o = orc.dispatch(idx, E)
     assert np.array_equal(out["offsets"].cpu().numpy(), o["offsets"])
-    assert np.array_equal(out["perm_token"].cpu().numpy(), o["perm_token"])
+    assert np.array_equal(out["perm_token"].cpu().numpy()[: T * K], o["perm_token"])
     assert np.array_equal(out["inv_row"].cpu().numpy(), o["inv_row"])
+    # shared-expert groups: S blocks of T rows, one per token
+    go = out["group_offsets"].cpu().numpy()
+    assert np.array_equal(go[: E + 1], o["offsets"])
+    assert np.array_equal(go[E:], T * K + T * np.arange(S + 1))
+    assert np.array_equal(out["perm_token"].cpu().numpy()[T * K:], np.tile(np.arange(T), S))
 
 
 def test_permute_bad_index_flagged(L):

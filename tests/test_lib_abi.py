@@ -58,7 +58,7 @@ def test_host_side_validation_needs_no_device(lib):
     # workspace too small, misaligned pointer
     assert L.moe_route(fake, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 16, None) == -6
     assert L.moe_route(fake + 8, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 1 << 20, None) == -3
-    assert L.moe_permute(fake, 4, 2, 8, fake, fake, fake, None, fake, 0, None) == -6
+    assert L.moe_permute(fake, 4, 2, 8, 1, fake, None, fake, fake, None, fake, 0, None) == -6
     # GEMM: bad mode, N not a multiple of 128, too many groups, null pointers
     assert L.moe_grouped_gemm_fp8(3, fake, fake, 8, fake, 1, fake, None, fake, None, 128, 128,
                                   fake, None, None, None) == -1
