@@ -13,6 +13,7 @@
 // equal scores broken by the lower expert index.  Near-tie flag: the K-th
 // and (K+1)-th biased scores differ by less than 1e-6.
 #include <cfloat>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -213,3 +214,71 @@ int launch_route(const uint16_t* u, const float* cent, const float* bias, int T,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free router entry point.
+//
+// Some callers cannot call cudaMalloc at the moment they route tokens: a
+// serving engine that hands all device memory to its own pool up front, a
+// runtime whose allocator is not reachable from the thread that launches
+// the layer, or code that must not allocate between two points it has
+// measured or captured.  moe_route_noalloc serves them: it takes no
+// workspace and keeps the [T, E] logits in a fixed array that lives in the
+// library's own device memory (every GPU that loads the library holds these
+// 4 MB until the process exits).
+//
+// In host code the array's name is only a host-side stand-in, so its device
+// address is looked up with cudaGetSymbolAddress, once per device, with that
+// device current, on the first call made there.  Every call shares the
+// array and it keeps the last call's contents: the split-K path clears the
+// logits before it accumulates into them, and two calls that overlap on the
+// GPU (different streams, or different host threads on one device) race on
+// it.
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocMaxLogits = size_t(1) << 20;     // T * E limit (4 MB of float32)
+static __device__ __align__(256) float g_noalloc_logits[kNoAllocMaxLogits];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_logits on the current device (set-up on first use).
+int noalloc_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED_SHAPE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_logits);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_route_noalloc(const uint16_t* u, const float* centroids, const float* bias,
+                                 int T, int d, int E, int K, int32_t* topk_idx, float* topk_gate,
+                                 uint8_t* tie_flag, int32_t* counts, void* stream) {
+    using namespace moe;
+    if (T < 0 || d <= 0 || E <= 0 || K <= 0 || K > E || K > kMaxTopK || E > kMaxExperts)
+        return MOE_ERR_INVALID_ARG;
+    if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!counts || !centroids || !bias) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!u || !topk_idx || !topk_gate || !tie_flag)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(centroids)) & 15u)
+        return MOE_ERR_MISALIGNED;
+    if ((size_t)T * (size_t)E > kNoAllocMaxLogits) return MOE_ERR_WORKSPACE;
+    float* logits = nullptr;
+    const int rc = noalloc_scratch(&logits);
+    if (rc) return rc;
+    return launch_route(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
+                        logits, static_cast<cudaStream_t>(stream));
+}

@@ -165,6 +165,29 @@ def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: i
     return out
 
 
+def moe_route_noalloc(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
+                      out: Optional[dict] = None, stream=None) -> dict:
+    """moe_route without a workspace (the logits use the library's fixed
+    device array; T * E <= 1048576; concurrent calls on one device race)."""
+    fn = _lib.moe_route_noalloc
+    fn.restype = I32
+    fn.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P, P, P]
+    _bits(u, torch.bfloat16)
+    _dev(u, "u")
+    T, d = u.shape
+    E = centroids.shape[0]
+    dev = u.device
+    if out is None:
+        out = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),
+               "gate": torch.empty((T, K), dtype=torch.float32, device=dev),
+               "tie": torch.empty((T,), dtype=torch.uint8, device=dev),
+               "counts": torch.empty((E,), dtype=torch.int32, device=dev)}
+    _check(fn(_ptr(u), _ptr(centroids), _ptr(bias), T, d, E, K, _ptr(out["idx"]),
+              _ptr(out["gate"]), _ptr(out["tie"]), _ptr(out["counts"]), _stream(stream)),
+           "moe_route_noalloc")
+    return out
+
+
 def moe_permute(topk_idx: torch.Tensor, E: int, S: int = 0, ws: Optional[torch.Tensor] = None,
                 status: Optional[torch.Tensor] = None, out: Optional[dict] = None,
                 stream=None) -> dict:

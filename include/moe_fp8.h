@@ -121,6 +121,23 @@ int moe_route(const uint16_t* u, const float* centroids, const float* bias, int 
               int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
               void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route without a workspace, for callers that cannot allocate device
+ * memory when they route (a serving engine whose memory pool owns the whole
+ * device, a runtime whose allocator is out of reach of the launching thread,
+ * or code that must not allocate between two points it measures or
+ * captures).  The pages have no counterpart of this call: it is a service of
+ * this library, not a step of the method.  Same arguments, outputs and
+ * arithmetic as moe_route, minus ws/ws_bytes; the [T, E] logits live in a
+ * fixed 4 MB array in the library's device memory, so T * E must be at most
+ * 1048576 (MOE_ERR_WORKSPACE otherwise).  The first call on each device looks
+ * up that array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Every call shares the array: calls that
+ * overlap on the GPU (other streams, other host threads) race on it.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library call). */
+int moe_route_noalloc(const uint16_t* u, const float* centroids, const float* bias, int T, int d,
+                      int E, int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag,
+                      int32_t* counts, void* stream);
+
 /* Dispatch layout ([YLY] §2.2: no token is dropped, so every (token, slot)
  * pair gets a row).  A stable counting sort of the T*K pairs by expert, plus
  * the rows of the S shared experts, which see every token:
