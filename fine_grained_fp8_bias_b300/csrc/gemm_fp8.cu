@@ -11,14 +11,19 @@
 // epilogue warps read it with tcgen05.ld and promote it in registers while
 // the tensor core fills the other buffer.
 //
-// Kernel shape (one persistent CTA per SM, 320 threads):
+// Kernel shape (one persistent CTA per SM, 384 threads = 3 warpgroups):
 //   warp 0      TMA producer: A tile [128 x 128] + B tile [256 x 128] per slab,
 //               STAGES-deep shared-memory ring, 128-byte swizzle.
 //   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma.kind::f8f6f4
 //               (M=128, N=256, K=32) per slab into TMEM buffer (slab & 1).
-//   warps 2..9  epilogue, two warpgroups; TMEM lane quarter = warp % 4, so
-//               thread (warp, lane) owns output row 32 * (warp % 4) + lane of
-//               the tile; warpgroup 0 / 1 own half of the 256 columns each.
+//   warp 2      scale loader: the 128 activation scales and the two weight
+//               scales of each slab go into a shared-memory ring, so the
+//               epilogue never waits on global memory.
+//   warp 3      idle.  Warpgroup 0 gives its registers away (setmaxnreg 40).
+//   warps 4..11 epilogue, two warpgroups with 232 registers per thread; TMEM
+//               lane quarter = warp % 4, so thread (warp, lane) owns output
+//               row 32 * (warp % 4) + lane of the tile; warpgroup 1 / 2 own
+//               half of the 256 columns each.
 // Output tile = 128 rows x 256 columns: in GATE_UP mode 128 gate columns and
 // the 128 up columns of the same intermediate indices (so SiLU(G) * U and
 // the 1x128 re-quantisation of h stay inside one tile), in DOWN mode 256
@@ -47,9 +52,25 @@ constexpr int SMEM_A = BM * BK;                 // 16 KB
 constexpr int SMEM_B = BN * BK;                 // 32 KB
 constexpr int SMEM_STAGE = SMEM_A + SMEM_B;     // 48 KB
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int EPI_WARP0 = 4;                    // first epilogue warp
+constexpr int NUM_THREADS = 128 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;             // 2 buffers x 256 fp32 columns
+constexpr int SCALE_SLOTS = 8;                  // depth of the scale ring
 constexpr unsigned long long WAIT_NS = 2000000000ull;
+// Register split: the kernel is compiled for 384 threads x 168 registers
+// (64512); warpgroup 0 drops to 40 and the two epilogue warpgroups rise to
+// 232: 128 * 40 + 256 * 232 = 64512.  Per SM sub-partition (warps w, w+4,
+// w+8): 40 + 232 + 232 = 504 = 3 * 168.  The host refuses to launch unless
+// the compiled register count is exactly LAUNCH_REGS.
+constexpr int LAUNCH_REGS = 168;
+constexpr int CTRL_REGS = 40;
+constexpr int EPI_REGS = 232;
+static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= NUM_THREADS * LAUNCH_REGS, "register split");
+
+struct alignas(16) ScaleSlot {
+    float sa[BM];                               // activation scale of each tile row
+    float sw[4];                                // weight scale of column half 0 and 1
+};
 
 struct alignas(16) Ctl {
     uint64_t full[STAGES];
@@ -57,11 +78,15 @@ struct alignas(16) Ctl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t xbar;                              // amax exchange between the epilogue warpgroups
+    uint64_t epi_done;                          // every epilogue warp finished with TMEM
+    uint64_t sfull[SCALE_SLOTS];
+    uint64_t sempty[SCALE_SLOTS];
     uint32_t tmem_base;
     int abort;
     int total_tiles;
     int pad;
     float amax_x[2][2][BM];                     // [tile parity][warpgroup][row]
+    ScaleSlot scales[SCALE_SLOTS];
     int go[kMaxGroups + 1];                     // group row offsets
     int tile_start[kMaxGroups + 1];             // first tile of each group
 };
@@ -116,7 +141,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait for the phase of `parity` to complete.  Returns false when
 // the wait ran out or another role has aborted.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
                                        int32_t* status) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = now_ns();
@@ -133,7 +158,7 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
 // Warp-uniform bounded wait: every lane observes the completed phase before
 // any lane goes on (the epilogue's tcgen05.ld is .sync.aligned), and all
 // lanes agree on giving up.
-__device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
                                        int32_t* status) {
     const int lane = threadIdx.x & 31;
     const unsigned long long t0 = now_ns();
@@ -154,10 +179,11 @@ __device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
     }
 }
 // Wait used on the way out: only bounded by time, ignores the abort flag.
-__device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity,
+                                           unsigned long long limit_ns = WAIT_NS) {
     const unsigned long long t0 = now_ns();
     while (!mbar_test(bar, parity))
-        if (now_ns() - t0 > WAIT_NS) return;
+        if (now_ns() - t0 > limit_ns) return;
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -213,19 +239,22 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
-// 16 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 consecutive fp32 TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Wait for this thread's outstanding TMEM loads.  The registers pass through
+// the asm as read-write operands, so no use of them can move above the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
+}
+// Orders a second load's registers after a preceding tmem_ld_wait.
+__device__ __forceinline__ void reg_after_wait(uint32_t (&r)[32]) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
 // ----------------------------------------------------------- tile lookup
@@ -246,6 +275,7 @@ __device__ __forceinline__ Tile find_tile(const Ctl* ctl, int G, int tile) {
 }
 
 // ---------------------------------------------------------------- kernel
+template <bool GATE_UP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB0,
@@ -257,8 +287,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const bool gate_up = p.mode == MOE_GEMM_GATE_UP_SILU_QUANT;
+    constexpr bool gate_up = GATE_UP;
     const int NT = gate_up ? p.N / 128 : (p.N + BN - 1) / BN;
+    const int NB = p.N / 128;
     const int KB = p.Kdim / BK;
     const int G = p.G;
 
@@ -294,7 +325,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_init(&ctl->tfull[b], 1);
                 mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
             }
+            for (int s = 0; s < SCALE_SLOTS; ++s) {
+                mbar_init(&ctl->sfull[s], 1);
+                mbar_init(&ctl->sempty[s], NUM_EPI_WARPS);
+            }
             mbar_init(&ctl->xbar, NUM_EPI_WARPS);
+            mbar_init(&ctl->epi_done, NUM_EPI_WARPS);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB0);
@@ -312,7 +348,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = ctl->tmem_base;
     const int total_tiles = ctl->total_tiles;
 
-    if (warp == 0) {
+    // Each warpgroup's role code sits under its own setmaxnreg, so the
+    // register allocator sees the budget of the region it is compiling.
+    if (warp < EPI_WARP0) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
+      // (role code of warpgroup 0 below is indented one level less than its scope)
+      if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
             uint32_t it = 0;
@@ -376,17 +417,69 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mma_commit(&ctl->tfull[buf]);
                 }
             }
-            // wait for the last MMAs before TMEM is released
+            // wait for the last MMAs, and for every epilogue warp to finish
+            // reading TMEM, before TMEM is released (both bounded)
             if (it > 0) mbar_drain(&ctl->tfull[(it - 1) & 1], ((it - 1) >> 1) & 1);
+            // (longer than any single wait, so an aborting epilogue is out first)
+            mbar_drain(&ctl->epi_done, 0, 3 * WAIT_NS);
         }
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS));
+    } else if (warp == 2) {
+        // ================= scale loader =================
+        // Slot j of the ring holds slab j's 128 activation scales (row order of
+        // the tile, 0 for rows outside the group) and the weight scale of each
+        // 128-column half of the output tile.
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            const Tile tl = find_tile(ctl, G, tile);
+            const int g0 = ctl->go[tl.g];
+            const int m_g = max(0, ctl->go[tl.g + 1] - g0);
+            const float* w0;
+            const float* w1;
+            if (gate_up) {
+                w0 = p.sw0 + ((size_t)tl.g * NB + tl.nt) * KB;
+                w1 = p.sw1 + ((size_t)tl.g * NB + tl.nt) * KB;
+            } else {
+                w0 = p.sw0 + ((size_t)tl.g * NB + tl.nt * 2) * KB;
+                w1 = (tl.nt * 2 + 1 < NB) ? w0 + KB : w0;
+            }
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int slot = it % SCALE_SLOTS;
+                const uint32_t ph = (it / SCALE_SLOTS) & 1;
+                bool got = true;
+                if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, ctl, p.status);
+                if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
+                ScaleSlot& sl = ctl->scales[slot];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = lane * 4 + j;
+                    const int lrow = tl.mt * BM + r;
+                    const int grow = g0 + lrow;
+                    sl.sa[r] = (lrow < m_g && grow < p.M_total)
+                                   ? __ldg(p.sa + (size_t)kb * p.M_total + grow) : 0.0f;
+                }
+                if (lane == 0) {
+                    sl.sw[0] = __ldg(w0 + kb);
+                    sl.sw[1] = __ldg(w1 + kb);
+                }
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sfull[slot]);
+            }
+        }
+      }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
         // ================= epilogue =================
-        const int ew = warp - 2;
+        const int ew = warp - EPI_WARP0;
         const int wg = ew >> 2;                   // column half
         const int quarter = warp & 3;             // TMEM lane quarter
         const int row = quarter * 32 + lane;      // row within the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const int NB = p.N / 128;
         uint32_t it = 0;
         int tcount = 0;
         bool ok = true;
@@ -397,42 +490,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int lrow = tl.mt * BM + row;
             const int grow = g0 + lrow;
             const bool valid = lrow < m_g && grow < p.M_total;
-            // weight-scale rows for this thread's column half
-            const float* swa;
-            const float* swb;
-            bool cols_valid = true;
-            if (gate_up) {
-                swa = p.sw0 + ((size_t)tl.g * NB + tl.nt) * KB;
-                swb = p.sw1 + ((size_t)tl.g * NB + tl.nt) * KB;
-            } else {
-                const int nb = tl.nt * 2 + wg;
-                cols_valid = nb < NB;
-                swa = p.sw0 + ((size_t)tl.g * NB + (cols_valid ? nb : 0)) * KB;
-                swb = swa;
-            }
+            const bool cols_valid = gate_up || tl.nt * 2 + wg < NB;
+            // TMEM columns of this thread's two 64-column chunks.  GATE_UP: gate
+            // cols wg*64 + [0,64) then up cols 128 + wg*64 + [0,64); DOWN: cols
+            // wg*128 + [0,128).
+            const uint32_t c0 = gate_up ? wg * 64 : wg * 128;
+            const uint32_t c1 = gate_up ? 128 + wg * 64 : wg * 128 + 64;
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
             for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int slot = it % SCALE_SLOTS;
+                if (!warp_wait(&ctl->sfull[slot], (it / SCALE_SLOTS) & 1, ctl, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const ScaleSlot& sl = ctl->scales[slot];
+                const float sa = sl.sa[row];
+                const float s_lo = sa * (gate_up ? sl.sw[0] : sl.sw[wg]);
+                const float s_hi = sa * (gate_up ? sl.sw[1] : sl.sw[wg]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+
                 const uint32_t buf = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
-                const float sa = valid ? p.sa[(size_t)kb * p.M_total + grow] : 0.0f;
-                const float s_lo = sa * swa[kb];
-                const float s_hi = sa * swb[kb];
-                if (!warp_wait(&ctl->tfull[buf], tph, ctl, p.status)) { ok = false; break; }
+                if (!warp_wait(&ctl->tfull[buf], (it >> 1) & 1, ctl, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + lane_addr + buf * BN;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    // GATE_UP: chunks 0-3 = gate cols wg*64 + [0,64), chunks 4-7 = up cols
-                    // 128 + wg*64 + [0,64).  DOWN: cols wg*128 + [0,128).
-                    const int col = gate_up ? (c < 4 ? wg * 64 + c * 16 : 128 + wg * 64 + (c - 4) * 16)
-                                            : wg * 128 + c * 16;
-                    float v[16];
-                    tmem_ld16(tbase + col, v);
-                    const float s = (gate_up && c >= 4) ? s_hi : s_lo;
+                for (int c = 0; c < 2; ++c) {
+                    // two 32-column loads in flight, one wait
+                    uint32_t a[32], b[32];
+                    const uint32_t col = c == 0 ? c0 : c1;
+                    tmem_ld32_nowait(tbase + col, a);
+                    tmem_ld32_nowait(tbase + col + 32, b);
+                    tmem_ld_wait(a);
+                    reg_after_wait(b);
+                    const float sc = c == 0 ? s_lo : s_hi;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(v[i], s, acc[c * 16 + i]);
+                    for (int i = 0; i < 32; ++i)
+                        acc[c * 64 + i] = fmaf(__uint_as_float(a[i]), sc, acc[c * 64 + i]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[c * 64 + 32 + i] = fmaf(__uint_as_float(b[i]), sc, acc[c * 64 + 32 + i]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -440,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok) break;
             // ---- tile finalisation
-            if (gate_up) {
+            if constexpr (gate_up) {
                 float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
@@ -494,17 +593,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-    }
-
-    // ---- teardown: every TMEM read and MMA is finished before the release
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
+        // this warp's TMEM reads are complete: warp 1 may release TMEM
+        tc_fence_before();
         __syncwarp();
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS));
+        if (lane == 0) mbar_arrive(&ctl->epi_done);
     }
+    // No code after the role branches: each role runs under its own register budget.
 }
 
 // ------------------------------------------------------------ host side
@@ -553,12 +647,24 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
+    static int num_regs[2] = {0, 0};
     std::call_once(once, [&] {
         cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-        cudaFuncSetAttribute(grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES);
+        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<true>) == cudaSuccess)
+            num_regs[1] = fa.numRegs;
+        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<false>) == cudaSuccess)
+            num_regs[0] = fa.numRegs;
     });
     if (sm_count <= 0) return cuda_fail(cudaErrorInvalidDevice);
+    // The warpgroups re-split the registers the CTA is launched with; launching
+    // with fewer than LAUNCH_REGS per thread would leave setmaxnreg.inc waiting.
+    const bool gu = mode == MOE_GEMM_GATE_UP_SILU_QUANT;
+    if (num_regs[gu ? 1 : 0] != LAUNCH_REGS) return cuda_fail(cudaErrorInvalidConfiguration);
     CUtensorMap mA, mB0, mB1;
     int rc = make_map(&mA, A, (uint64_t)M_total, (uint64_t)Kdim);
     if (rc) return rc;
@@ -574,7 +680,10 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
     const int NT = mode == MOE_GEMM_GATE_UP_SILU_QUANT ? N / 128 : (N + BN - 1) / BN;
     const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NT;
     const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);
-    grouped_gemm_fp8_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
+    if (gu)
+        grouped_gemm_fp8_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
+    else
+        grouped_gemm_fp8_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
     return check_launch();
 }
 

@@ -166,7 +166,11 @@ V3_DECODE = LayerConfig("v3_decode", T=256, d=7168, E=256, K=8, S=1, I=2048, see
 V3_LONG = LayerConfig("v3_long", T=32768, d=7168, E=256, K=8, S=1, I=2048, seed=4,
                       tokens="mixture4")
 
-CONFIGS = {c.name: c for c in (TINY, MID, V3_PREFILL, V3_DECODE, V3_LONG)}
+# Profiling-size slice of the V3 prefill batch: the same expert shapes and the
+# same rows per expert (T*K/E = 128), 32 routed experts (1.45 GB of weights).
+V3_SLICE = LayerConfig("v3_slice", T=512, d=7168, E=32, K=8, S=1, I=2048, seed=5)
+
+CONFIGS = {c.name: c for c in (TINY, MID, V3_PREFILL, V3_DECODE, V3_LONG, V3_SLICE)}
 
 
 def tokens(cfg: LayerConfig, device="cpu", step: int = 0) -> torch.Tensor:
