@@ -122,7 +122,8 @@ class Step:
         self.T, self.M = T, T * (K + S)
         dev = u.device
         M = self.M
-        self.route_ws = torch.empty(max(4 * T * E, 256), dtype=torch.uint8, device=dev)
+        self.route_ws = torch.empty(lib.route_workspace_bytes(T, E, d), dtype=torch.uint8,
+                                    device=dev)
         nchunks = (T + 63) // 64
         self.perm_ws = torch.empty(2 * ((4 * nchunks * E + 255) // 256 * 256) + 256,
                                    dtype=torch.uint8, device=dev)
@@ -150,8 +151,8 @@ class Step:
             lib.moe_permute(self.rout["idx"], L.E, L.S, ws=self.perm_ws, status=self.status,
                             out=self.pout)
         elif name == "quant":
-            lib.moe_quant_1x128(self.u, self.pout["perm_token"], M=self.M, q=self.A,
-                                scales=self.sa, status=self.status)
+            lib.moe_quant_1x128_dispatch(self.u, self.pout["inv_row"], L.K, L.S, q=self.A,
+                                         scales=self.sa, status=self.status)
         elif name == "gemm_gate_up":
             lib.moe_grouped_gemm_fp8(lib.MOE_GEMM_GATE_UP_SILU_QUANT, self.A, self.sa,
                                      self.pout["group_offsets"], L.w_gate, L.w_up, L.s_gate,

@@ -15,7 +15,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Workspace layout shared by moe_forward, moe_route and moe_permute.
 struct Layout {
-    size_t status, logits, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
+    size_t status, logits, csplit, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
 };
 
 Layout layout(int T, int d, int E, int K, int S, int I) {
@@ -30,6 +30,7 @@ Layout layout(int T, int d, int E, int K, int S, int I) {
     const size_t nchunks = ((size_t)T + kPermuteChunk - 1) / kPermuteChunk;
     L.status = take(16);
     L.logits = take(sizeof(float) * (size_t)T * E);
+    L.csplit = take(sizeof(uint16_t) * 3 * (size_t)E * d);
     L.hist = take(sizeof(int32_t) * nchunks * E);
     L.base = take(sizeof(int32_t) * nchunks * E);
     L.go = take(sizeof(int32_t) * (size_t)(E + S + 1));
@@ -61,6 +62,10 @@ int check_layer(const moe_layer_t* L) {
 }
 
 inline cudaStream_t S_(void* s) { return static_cast<cudaStream_t>(s); }
+
+// moe_route's workspace: T*E float32 logits, then (256-byte aligned) the
+// 3*E*d bfloat16 centroid pieces.
+size_t route_split_offset(int T, int E) { return align_up(sizeof(float) * (size_t)T * E, 256); }
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -117,6 +122,19 @@ int moe_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather_rows, in
                               scale_ld, status, S_(stream));
 }
 
+int moe_quant_1x128_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_row, int K,
+                             int S, uint8_t* q, float* scales, int scale_ld, int32_t* status,
+                             void* stream) {
+    if (T < 0 || d <= 0 || K < 0 || S < 0 || K + S > 32 || K + S == 0) return MOE_ERR_INVALID_ARG;
+    if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)T * (K + S) > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (scale_ld < T * (K + S)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !q || !scales || (K > 0 && !inv_row)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q)) return MOE_ERR_MISALIGNED;
+    return launch_quant_dispatch(x, T, d, inv_row, K, S, q, scales, scale_ld, status, S_(stream));
+}
+
 int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, void* stream) {
     if (R < 0 || C < 0) return MOE_ERR_INVALID_ARG;
     if (R % 128 || C % 128 || R / 128 > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -134,10 +152,13 @@ int moe_route(const uint16_t* u, const float* centroids, const float* bias, int 
     if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!counts || !centroids || !bias) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!u || !topk_idx || !topk_gate || !tie_flag || !ws)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(u) || !aligned16(centroids) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
-    if (ws_bytes < sizeof(float) * (size_t)T * E) return MOE_ERR_WORKSPACE;
+    if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    const size_t split_at = route_split_offset(T, E);
+    if (ws_bytes < split_at + sizeof(uint16_t) * 3 * (size_t)E * d) return MOE_ERR_WORKSPACE;
     return launch_route(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
-                        static_cast<float*>(ws), S_(stream));
+                        static_cast<float*>(ws), S_(stream),
+                        reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + split_at));
 }
 
 int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* offsets,
@@ -208,6 +229,7 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     const cudaStream_t st = S_(stream);
     int32_t* status = reinterpret_cast<int32_t*>(base + W.status);
     float* logits = reinterpret_cast<float*>(base + W.logits);
+    uint16_t* csplit = reinterpret_cast<uint16_t*>(base + W.csplit);
     int32_t* hist = reinterpret_cast<int32_t*>(base + W.hist);
     int32_t* bbase = reinterpret_cast<int32_t*>(base + W.base);
     int32_t* go = reinterpret_cast<int32_t*>(base + W.go);
@@ -224,13 +246,13 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
     if (e != cudaSuccess) return cuda_fail(e);
     if ((rc = launch_route(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
-                           counts, logits, st)))
+                           counts, logits, st, csplit, status)))
         return rc;
     if (T == 0) return MOE_OK;
     if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,
                              st)))
         return rc;
-    if ((rc = launch_quant_1x128(u, T, perm, M, 1, M, d, A, sa, M, status, st))) return rc;
+    if ((rc = launch_quant_dispatch(u, T, d, inv_row, K, S, A, sa, M, status, st))) return rc;
     if ((rc = launch_grouped_gemm(MOE_GEMM_GATE_UP_SILU_QUANT, A, sa, M, go, G, L->w_gate,
                                   L->w_up, L->s_gate, L->s_up, I, d, H, sh, status, st)))
         return rc;

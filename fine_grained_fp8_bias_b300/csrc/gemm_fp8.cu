@@ -33,16 +33,18 @@
 // at the same time share the weight slab of one (group, N tile) and the A
 // rows of one group through L2, so each weight byte is read from HBM once.
 //
-// Every wait is bounded (about 2 s); on expiry the kernel records
+// Every wait is bounded (about 2 s of SM clock); on expiry the kernel records
 // MOE_ERR_TIMEOUT in the status word, every role stops, in-flight copies and
 // MMAs are waited for (again bounded) and TMEM is released before exit.
 #include <cuda.h>
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 128;
@@ -56,7 +58,6 @@ constexpr int EPI_WARP0 = 4;                    // first epilogue warp
 constexpr int NUM_THREADS = 128 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;             // 2 buffers x 256 fp32 columns
 constexpr int SCALE_SLOTS = 8;                  // depth of the scale ring
-constexpr unsigned long long WAIT_NS = 2000000000ull;
 // Register split: the kernel is compiled for 384 threads x 168 registers
 // (64512); warpgroup 0 drops to 40 and the two epilogue warpgroups rise to
 // 232: 128 * 40 + 256 * 232 = 64512.  Per SM sub-partition (warps w, w+4,
@@ -107,155 +108,6 @@ struct Params {
     float* out_scales;
     int32_t* status;
 };
-
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long now_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase of `parity` to complete.  Returns false when
-// the wait ran out or another role has aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
-                                       int32_t* status) {
-    if (mbar_test(bar, parity)) return true;
-    const unsigned long long t0 = now_ns();
-    for (;;) {
-        if (mbar_test(bar, parity)) return true;
-        if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-        if (now_ns() - t0 > WAIT_NS) {
-            atomicExch(&ctl->abort, 1);
-            flag_status(status, MOE_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-// Warp-uniform bounded wait: every lane observes the completed phase before
-// any lane goes on (the epilogue's tcgen05.ld is .sync.aligned), and all
-// lanes agree on giving up.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Ctl* ctl,
-                                       int32_t* status) {
-    const int lane = threadIdx.x & 31;
-    const unsigned long long t0 = now_ns();
-    for (;;) {
-        const bool ready = mbar_test(bar, parity);
-        if (__all_sync(0xffffffffu, ready)) return true;
-        int stop = 0;
-        if (lane == 0) {
-            if (*reinterpret_cast<volatile int*>(&ctl->abort)) {
-                stop = 1;
-            } else if (now_ns() - t0 > WAIT_NS) {
-                atomicExch(&ctl->abort, 1);
-                flag_status(status, MOE_ERR_TIMEOUT);
-                stop = 1;
-            }
-        }
-        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-}
-// Wait used on the way out: only bounded by time, ignores the abort flag.
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity,
-                                           unsigned long long limit_ns = WAIT_NS) {
-    const unsigned long long t0 = now_ns();
-    while (!mbar_test(bar, parity))
-        if (now_ns() - t0 > limit_ns) return;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand tile written by TMA
-// with 128-byte swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024
-// bytes stacked along M/N (stride byte offset 1024), descriptor version 1,
-// layout type 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
-// Instruction descriptor of tcgen05.mma.kind::f8f6f4: D float32 (bits 4-5 =
-// 1), A and B E4M3 (format 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-// 32 consecutive fp32 TMEM columns of this thread's lane (no wait).
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-// Wait for this thread's outstanding TMEM loads.  The registers pass through
-// the asm as read-write operands, so no use of them can move above the wait.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
-}
-// Orders a second load's registers after a preceding tmem_ld_wait.
-__device__ __forceinline__ void reg_after_wait(uint32_t (&r)[32]) {
-    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
-}
 
 // ----------------------------------------------------------- tile lookup
 struct Tile {
@@ -326,7 +178,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
             }
             for (int s = 0; s < SCALE_SLOTS; ++s) {
-                mbar_init(&ctl->sfull[s], 1);
+                mbar_init(&ctl->sfull[s], 32);   // one asynchronous arrival per loader lane
                 mbar_init(&ctl->sempty[s], NUM_EPI_WARPS);
             }
             mbar_init(&ctl->xbar, NUM_EPI_WARPS);
@@ -376,7 +228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
-                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, ctl, p.status)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, &ctl->abort, p.status)) { ok = false; break; }
                     uint8_t* sA = smem + (size_t)s * SMEM_STAGE;
                     uint8_t* sB = sA + SMEM_A;
                     mbar_expect_tx(&ctl->full[s], bytes);
@@ -403,8 +255,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t ph = (it / STAGES) & 1;
                     const uint32_t buf = it & 1;
                     const uint32_t tph = (it >> 1) & 1;
-                    if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, ctl, p.status)) { ok = false; break; }
-                    if (!mbar_wait(&ctl->full[s], ph, ctl, p.status)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, &ctl->abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->full[s], ph, &ctl->abort, p.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smem + (size_t)s * SMEM_STAGE);
                     const uint32_t b0 = a0 + SMEM_A;
@@ -421,7 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // reading TMEM, before TMEM is released (both bounded)
             if (it > 0) mbar_drain(&ctl->tfull[(it - 1) & 1], ((it - 1) >> 1) & 1);
             // (longer than any single wait, so an aborting epilogue is out first)
-            mbar_drain(&ctl->epi_done, 0, 3 * WAIT_NS);
+            mbar_drain(&ctl->epi_done, 0, 3 * WAIT_CYCLES);
         }
         __syncwarp();
         tc_fence_after();
@@ -451,26 +303,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int slot = it % SCALE_SLOTS;
                 const uint32_t ph = (it / SCALE_SLOTS) & 1;
                 bool got = true;
-                if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, ctl, p.status);
+                if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, &ctl->abort, p.status);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
+                // 4-byte asynchronous copies; rows outside the group are zero-filled
+                // (source size 0).  Each lane's copies arrive on sfull when they land,
+                // so the loader never waits for global memory and runs up to
+                // SCALE_SLOTS slabs ahead.
                 ScaleSlot& sl = ctl->scales[slot];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int r = lane * 4 + j;
                     const int lrow = tl.mt * BM + r;
                     const int grow = g0 + lrow;
-                    sl.sa[r] = (lrow < m_g && grow < p.M_total)
-                                   ? __ldg(p.sa + (size_t)kb * p.M_total + grow) : 0.0f;
+                    const bool v = lrow < m_g && grow < p.M_total;
+                    const float* src = v ? p.sa + (size_t)kb * p.M_total + grow : p.sa;
+                    cp_async4(&sl.sa[r], src, v ? 4u : 0u);
                 }
                 if (lane == 0) {
-                    sl.sw[0] = __ldg(w0 + kb);
-                    sl.sw[1] = __ldg(w1 + kb);
+                    cp_async4(&sl.sw[0], w0 + kb, 4u);
+                    cp_async4(&sl.sw[1], w1 + kb, 4u);
                 }
-                __threadfence_block();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->sfull[slot]);
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                                 smem_u32(&ctl->sfull[slot]))
+                             : "memory");
             }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
@@ -499,43 +357,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int slot = it % SCALE_SLOTS;
-                if (!warp_wait(&ctl->sfull[slot], (it / SCALE_SLOTS) & 1, ctl, p.status)) {
-                    ok = false;
-                    break;
-                }
+            // Software pipeline over the four 32-column chunks of a slab: the load
+            // of chunk j+1 is in flight while chunk j is promoted, the TMEM buffer
+            // is released as soon as its last chunk is in registers, and the next
+            // slab's first chunk loads while this slab's last chunk is promoted.
+            uint32_t a[32], b[32];
+            float s_lo = 0.0f, s_hi = 0.0f;
+            // scales of slab `it` from the ring; false when the wait gave up
+            auto take_scales = [&](uint32_t i, float& lo, float& hi) -> bool {
+                const int slot = i % SCALE_SLOTS;
+                if (!warp_wait(&ctl->sfull[slot], (i / SCALE_SLOTS) & 1, &ctl->abort, p.status)) return false;
                 const ScaleSlot& sl = ctl->scales[slot];
                 const float sa = sl.sa[row];
-                const float s_lo = sa * (gate_up ? sl.sw[0] : sl.sw[wg]);
-                const float s_hi = sa * (gate_up ? sl.sw[1] : sl.sw[wg]);
+                lo = sa * (gate_up ? sl.sw[0] : sl.sw[wg]);
+                hi = sa * (gate_up ? sl.sw[1] : sl.sw[wg]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
-
-                const uint32_t buf = it & 1;
-                if (!warp_wait(&ctl->tfull[buf], (it >> 1) & 1, ctl, p.status)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t tbase = tmem_base + lane_addr + buf * BN;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    // two 32-column loads in flight, one wait
-                    uint32_t a[32], b[32];
-                    const uint32_t col = c == 0 ? c0 : c1;
-                    tmem_ld32_nowait(tbase + col, a);
-                    tmem_ld32_nowait(tbase + col + 32, b);
+                return true;
+            };
+            if (KB > 0) {
+                if (!take_scales(it, s_lo, s_hi) ||
+                    !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status)) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    tmem_ld32_nowait(tmem_base + lane_addr + (it & 1) * BN + c0, a);
                     tmem_ld_wait(a);
-                    reg_after_wait(b);
-                    const float sc = c == 0 ? s_lo : s_hi;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[c * 64 + i] = fmaf(__uint_as_float(a[i]), sc, acc[c * 64 + i]);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[c * 64 + 32 + i] = fmaf(__uint_as_float(b[i]), sc, acc[c * 64 + 32 + i]);
                 }
+            }
+            for (int kb = 0; ok && kb < KB; ++kb, ++it) {
+                const uint32_t tbase = tmem_base + lane_addr + (it & 1) * BN;
+                tmem_ld32_nowait(tbase + c0 + 32, b);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(a[i]), s_lo, acc[i]);
+                tmem_ld_wait(b);
+                tmem_ld32_nowait(tbase + c1, a);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(__uint_as_float(b[i]), s_lo, acc[32 + i]);
+                tmem_ld_wait(a);
+                tmem_ld32_nowait(tbase + c1 + 32, b);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(__uint_as_float(a[i]), s_hi, acc[64 + i]);
+                tmem_ld_wait(b);
+                // the whole slab is in registers: hand the TMEM buffer back
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                if (lane == 0) mbar_arrive(&ctl->tempty[it & 1]);
+                const float last_hi = s_hi;
+                if (kb + 1 < KB) {
+                    if (!take_scales(it + 1, s_lo, s_hi) ||
+                        !warp_wait(&ctl->tfull[(it + 1) & 1], ((it + 1) >> 1) & 1, &ctl->abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tmem_ld32_nowait(tmem_base + lane_addr + ((it + 1) & 1) * BN + c0, a);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[96 + i] = fmaf(__uint_as_float(b[i]), last_hi, acc[96 + i]);
+                if (kb + 1 < KB) tmem_ld_wait(a);
             }
             if (!ok) break;
             // ---- tile finalisation
@@ -556,7 +436,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->xbar);
-                if (!warp_wait(&ctl->xbar, (uint32_t)par, ctl, p.status)) { ok = false; break; }
+                if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status)) { ok = false; break; }
                 amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
                 const float scale = tile_scale(amax);
                 if (valid) {
@@ -602,39 +482,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-// 2-D uint8 tensor [rows, cols] (cols contiguous), box 128 x 128, 128-byte swizzle.
-int make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc) return cuda_fail(cudaErrorNotSupported);
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {128, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? MOE_OK : cuda_fail(cudaErrorInvalidValue);
-}
-
 }  // namespace
 
 int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
@@ -666,12 +513,12 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
     const bool gu = mode == MOE_GEMM_GATE_UP_SILU_QUANT;
     if (num_regs[gu ? 1 : 0] != LAUNCH_REGS) return cuda_fail(cudaErrorInvalidConfiguration);
     CUtensorMap mA, mB0, mB1;
-    int rc = make_map(&mA, A, (uint64_t)M_total, (uint64_t)Kdim);
+    int rc = make_map_2d(&mA, A, (uint64_t)M_total, (uint64_t)Kdim, 1, 128, 128);
     if (rc) return rc;
-    rc = make_map(&mB0, W0, (uint64_t)G * N, (uint64_t)Kdim);
+    rc = make_map_2d(&mB0, W0, (uint64_t)G * N, (uint64_t)Kdim, 1, 128, 128);
     if (rc) return rc;
     if (mode == MOE_GEMM_GATE_UP_SILU_QUANT) {
-        rc = make_map(&mB1, W1, (uint64_t)G * N, (uint64_t)Kdim);
+        rc = make_map_2d(&mB1, W1, (uint64_t)G * N, (uint64_t)Kdim, 1, 128, 128);
         if (rc) return rc;
     } else {
         mB1 = mB0;

@@ -72,6 +72,71 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(
     }
 }
 
+// Quantise every token once and write its codes to all the rows the
+// dispatch gave it: routed rows inv_row[t, 0..K) and shared rows
+// T*K + s*T + t.  One warp per token; each lane owns 8 consecutive values of
+// a 256-wide step (a half-warp per 128-wide tile), exactly as
+// quant_1x128_kernel, so codes and scales are the same bits.
+__global__ void __launch_bounds__(256) quant_dispatch_kernel(
+    const uint16_t* __restrict__ x, int T, int d, const int32_t* __restrict__ inv_row, int K,
+    int S, int M, uint8_t* __restrict__ q, float* __restrict__ scales, int scale_ld,
+    int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int warps_per_block = blockDim.x >> 5;
+    const int half = lane >> 4;
+    const int hl = lane & 15;
+    for (int t = blockIdx.x * warps_per_block + (threadIdx.x >> 5); t < T;
+         t += gridDim.x * warps_per_block) {
+        // lane j < K holds routed row j of this token, lane K + s shared row s
+        int my_row = -1;
+        if (lane < K) {
+            my_row = inv_row[(size_t)t * K + lane];
+            if (my_row < 0 || my_row >= M) {
+                flag_status(status, MOE_ERR_BAD_INDEX);
+                my_row = -1;
+            }
+        } else if (lane < K + S) {
+            my_row = T * K + (lane - K) * T + t;
+        }
+        const int R = K + S;
+        const uint16_t* xr = x + (size_t)t * d;
+        for (int c0 = 0; c0 < d; c0 += 256) {
+            const int col = c0 + half * 128 + hl * 8;
+            const bool active = col < d;
+            float v[8];
+            float amax = 0.0f;
+            if (active) {
+                uint4 raw = *reinterpret_cast<const uint4*>(xr + col);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
+                    v[2 * i + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const float scale = tile_scale(amax);
+            uint2 out = make_uint2(0u, 0u);
+            if (active && amax != 0.0f) {
+                out.x = quant4(v[0], v[1], v[2], v[3], scale);
+                out.y = quant4(v[4], v[5], v[6], v[7], scale);
+            }
+            for (int j = 0; j < R; ++j) {
+                const int row = __shfl_sync(0xffffffffu, my_row, j);
+                if (row < 0) continue;
+                if (active) {
+                    *reinterpret_cast<uint2*>(q + (size_t)row * d + col) = out;
+                    if (hl == 0) scales[(size_t)(col >> 7) * scale_ld + row] = scale;
+                }
+            }
+        }
+    }
+}
+
 // One block quantises one 128x128 weight block: 256 threads, 64 values each.
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ w, int R,
                                                             int C, uint8_t* __restrict__ q,
@@ -121,6 +186,18 @@ int launch_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather, int 
     quant_1x128_kernel<<<blocks, warps * 32, 0, st>>>(x, n_src, gather, n_gather,
                                                        tail_T > 0 ? tail_T : 1, M, d, q, scales,
                                                        scale_ld, status);
+    return check_launch();
+}
+
+int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_row, int K, int S,
+                          uint8_t* q, float* scales, int scale_ld, int32_t* status,
+                          cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    const int warps = 8;
+    int blocks = (T + warps - 1) / warps;
+    if (blocks > 148 * 16) blocks = 148 * 16;
+    quant_dispatch_kernel<<<blocks, warps * 32, 0, st>>>(x, T, d, inv_row, K, S, T * (K + S), q,
+                                                          scales, scale_ld, status);
     return check_launch();
 }
 

@@ -7,15 +7,22 @@
 // "Auxiliary-Loss-Free Load Balancing": the bias b_i only steers which
 // experts are chosen; the gate values use the unbiased s.
 //
-// Two kernels: a float32 GEMM for the logits l = u E^T (CUDA cores, exact
-// products of bf16 x fp32, float32 accumulation), then one warp per token
-// for sigmoid, selection and gates.  Selection order: descending s + b,
-// equal scores broken by the lower expert index.  Near-tie flag: the K-th
-// and (K+1)-th biased scores differ by less than 1e-6.
+// Logits l = u E^T run on the tensor cores: every float32 centroid value c
+// is split exactly into three bfloat16 pieces (hi = bf16(c), mid =
+// bf16(c - hi), lo = c - hi - mid; 3 x 8 significand bits hold all 24 of
+// float32), the bfloat16 token rows are used as they are, and a
+// tcgen05.mma.kind::f16 GEMM sums the exact products in float32 TMEM over
+// the whole of d; the epilogue adds the three pieces of each expert.  A
+// float32 CUDA-core GEMM (logits_kernel) serves callers without the split
+// workspace.  Then one warp per token does sigmoid, selection and gates.
+// Selection order: descending s + b, equal scores broken by the lower expert
+// index.  Near-tie flag: the K-th and (K+1)-th biased scores differ by less
+// than 1e-6.
 #include <cfloat>
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -106,6 +113,173 @@ __global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict_
     }
 }
 
+
+// ------------------------------------------------------- tensor-core logits
+constexpr int RT_M = 128;                 // tokens per tile
+constexpr int RT_EXP = 64;                // experts per tile
+constexpr int RT_N = 3 * RT_EXP;          // MMA N: three pieces per expert
+constexpr int RT_K = 64;                  // bf16 elements per 128-byte smem row
+constexpr int RT_STAGES = 4;
+constexpr int RT_SMEM_A = RT_M * 128;
+constexpr int RT_SMEM_B = RT_N * 128;
+constexpr int RT_STAGE = RT_SMEM_A + RT_SMEM_B;
+constexpr int RT_THREADS = 192;           // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr uint32_t RT_TMEM_COLS = 256;
+
+struct alignas(8) RtCtl {
+    uint64_t full[RT_STAGES];
+    uint64_t empty[RT_STAGES];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t RT_SMEM_BYTES = 1024 + (size_t)RT_STAGES * RT_STAGE + sizeof(RtCtl);
+
+// c = hi + mid + lo exactly (float32 subtractions of a value and its
+// bfloat16 rounding are exact).  out row 3e + j holds piece j of expert e.
+__global__ void split_centroids_kernel(const float* __restrict__ c, int E, int d,
+                                       __nv_bfloat16* __restrict__ out) {
+    const size_t n = (size_t)E * d;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float v = c[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+        const size_t e = i / d, j = i % d;
+        out[(3 * e + 0) * d + j] = hi;
+        out[(3 * e + 1) * d + j] = mid;
+        out[(3 * e + 2) * d + j] = lo;
+    }
+}
+
+// One tile of 128 tokens x 64 experts over the k-steps [kb0, kb1) of d.
+// split > 1: partial sums are added atomically into a zeroed l.
+__global__ void __launch_bounds__(RT_THREADS, 1)
+    logits_tc_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
+                     int T, int d, int E, int split, float* __restrict__ l, int32_t* status) {
+    using namespace tc;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    RtCtl* ctl = reinterpret_cast<RtCtl*>(smem + (size_t)RT_STAGES * RT_STAGE);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * RT_M, e0 = blockIdx.y * RT_EXP;
+    const int steps = d / RT_K;
+    const int kb0 = (int)((long long)steps * blockIdx.z / split);
+    const int kb1 = (int)((long long)steps * (blockIdx.z + 1) / split);
+
+    if (warp == 0 && lane == 0) {
+        ctl->abort = 0;
+        for (int s = 0; s < RT_STAGES; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmU);
+        tma_prefetch_desc(&tmC);
+    } else if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&ctl->tmem_base)),
+                     "r"(RT_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % RT_STAGES;
+                if (!mbar_wait(&ctl->empty[s], ((it / RT_STAGES) & 1) ^ 1, &ctl->abort, status)) break;
+                uint8_t* sA = smem + (size_t)s * RT_STAGE;
+                mbar_expect_tx(&ctl->full[s], RT_STAGE);
+                tma_load_2d(sA, &tmU, &ctl->full[s], kb * RT_K, t0);
+                tma_load_2d(sA + RT_SMEM_A, &tmC, &ctl->full[s], kb * RT_K, 3 * e0);
+            }
+            const uint32_t first = it > (uint32_t)RT_STAGES ? it - RT_STAGES : 0;
+            for (uint32_t j = first; j < it; ++j) mbar_drain(&ctl->full[j % RT_STAGES], (j / RT_STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(RT_M, RT_N);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % RT_STAGES;
+                if (!mbar_wait(&ctl->full[s], (it / RT_STAGES) & 1, &ctl->abort, status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smem + (size_t)s * RT_STAGE);
+                const uint32_t b0 = a0 + RT_SMEM_A;
+#pragma unroll
+                for (int k = 0; k < RT_K / 16; ++k)
+                    mma_bf16(tmem_base, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                             (kb > kb0 || k > 0) ? 1u : 0u);
+                mma_commit(&ctl->empty[s]);
+            }
+            // committed in every case, so teardown can wait for the MMAs in flight
+            mma_commit(&ctl->done);
+            if (!ok) atomicExch(&ctl->abort, 1);
+        }
+    } else {
+        // epilogue: thread (warp, lane) owns token row 32 * (warp % 4) + lane
+        const int quarter = warp & 3;
+        const int t = t0 + quarter * 32 + lane;
+        if (warp_wait(&ctl->done, 0, &ctl->abort, status)) {
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < RT_N / 96; ++c) {
+                // 96 columns = 32 experts x 3 pieces
+                uint32_t a[32], b[32], g[32];
+                tmem_ld32_nowait(tbase + c * 96, a);
+                tmem_ld32_nowait(tbase + c * 96 + 32, b);
+                tmem_ld32_nowait(tbase + c * 96 + 64, g);
+                tmem_ld_wait(a);
+                reg_after_wait(b);
+                reg_after_wait(g);
+                float v[96];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = __uint_as_float(a[i]);
+                    v[32 + i] = __uint_as_float(b[i]);
+                    v[64 + i] = __uint_as_float(g[i]);
+                }
+                if (t < T) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = e0 + c * 32 + j;
+                        if (e < E) {
+                            const float x = (v[3 * j] + v[3 * j + 1]) + v[3 * j + 2];
+                            if (split > 1)
+                                atomicAdd(&l[(size_t)t * E + e], x);
+                            else
+                                l[(size_t)t * E + e] = x;
+                        }
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        // every MMA has completed (done, or the drained empty barriers) and every
+        // TMEM read is finished before the release
+        if (lane == 0) mbar_drain(&ctl->done, 0);
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(RT_TMEM_COLS));
+    }
+}
+
 // Larger score first; equal scores: lower expert index first.
 __device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
     return za > zb || (za == zb && ia < ib);
@@ -188,21 +362,48 @@ void launch_topk_nv(const float* l, const float* bias, int T, int E, int K, int3
 
 int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                  int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
-                 cudaStream_t st) {
+                 cudaStream_t st, uint16_t* cent_split, int32_t* status) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (e != cudaSuccess) return cuda_fail(e);
     if (T == 0) return MOE_OK;
-    const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
-    int split = 1;
-    const int target = 2 * 148;
-    while (gx * gy * split < target && split * 2 <= d / LK / 4) split *= 2;
-    if (split > 1) {
-        e = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
-        if (e != cudaSuccess) return cuda_fail(e);
+    int rc;
+    if (cent_split) {
+        // tensor-core logits
+        static std::once_flag once;
+        std::call_once(once, [] {
+            cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)RT_SMEM_BYTES);
+        });
+        __nv_bfloat16* cs = reinterpret_cast<__nv_bfloat16*>(cent_split);
+        split_centroids_kernel<<<148 * 4, 256, 0, st>>>(cent, E, d, cs);
+        if ((rc = check_launch())) return rc;
+        CUtensorMap mU, mC;
+        if ((rc = tc::make_map_2d(&mU, u, (uint64_t)T, (uint64_t)d, 2, RT_M, RT_K))) return rc;
+        if ((rc = tc::make_map_2d(&mC, cs, (uint64_t)3 * E, (uint64_t)d, 2, RT_N, RT_K))) return rc;
+        const int gx = (T + RT_M - 1) / RT_M, gy = (E + RT_EXP - 1) / RT_EXP;
+        const int steps = d / RT_K;
+        int split = 1;
+        while (gx * gy * split * 2 <= 2 * 148 && split * 2 <= steps / 4 && gx * gy * split < 74)
+            split *= 2;
+        if (split > 1) {
+            e = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        logits_tc_kernel<<<dim3(gx, gy, split), RT_THREADS, RT_SMEM_BYTES, st>>>(
+            mU, mC, T, d, E, split, logits, status);
+        if ((rc = check_launch())) return rc;
+    } else {
+        const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
+        int split = 1;
+        const int target = 2 * 148;
+        while (gx * gy * split < target && split * 2 <= d / LK / 4) split *= 2;
+        if (split > 1) {
+            e = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        logits_kernel<<<dim3(gx, gy, split), 256, 0, st>>>(u, cent, T, d, E, split, logits);
+        if ((rc = check_launch())) return rc;
     }
-    logits_kernel<<<dim3(gx, gy, split), 256, 0, st>>>(u, cent, T, d, E, split, logits);
-    int rc = check_launch();
-    if (rc) return rc;
     const int nv = (E + 31) / 32;
     if (nv <= 1) launch_topk_nv<1>(logits, bias, T, E, K, idx, gate, tie, counts, st);
     else if (nv <= 2) launch_topk_nv<2>(logits, bias, T, E, K, idx, gate, tie, counts, st);

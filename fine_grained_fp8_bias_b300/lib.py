@@ -53,6 +53,7 @@ def _load() -> ctypes.CDLL:
     sigs = {
         "moe_quant_1x128": [P, I32, P, I32, I32, P, P, I32, P, P],
         "moe_quant_128x128": [P, I32, I32, P, P, P],
+        "moe_quant_1x128_dispatch": [P, I32, I32, P, I32, I32, P, P, I32, P, P],
         "moe_route": [P, P, P, I32, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_permute": [P, I32, I32, I32, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_grouped_gemm_fp8": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
@@ -130,6 +131,26 @@ def moe_quant_1x128(x: torch.Tensor, gather_rows: Optional[torch.Tensor] = None,
     return q, scales
 
 
+def moe_quant_1x128_dispatch(x: torch.Tensor, inv_row: Optional[torch.Tensor], K: int, S: int,
+                             q: Optional[torch.Tensor] = None,
+                             scales: Optional[torch.Tensor] = None,
+                             status: Optional[torch.Tensor] = None, stream=None):
+    """x bf16 [T, d] -> (q uint8 [T*(K+S), d], scales float32 [d/128, T*(K+S)]), each token
+    quantised once and written to its routed rows inv_row[t] and its shared rows."""
+    _bits(x, torch.bfloat16)
+    _dev(x, "x")
+    T, d = x.shape
+    M = T * (K + S)
+    if q is None:
+        q = torch.empty((M, d), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((d // 128, M), dtype=torch.float32, device=x.device)
+    _check(_lib.moe_quant_1x128_dispatch(_ptr(x), T, d, _ptr(inv_row), K, S, _ptr(q),
+                                         _ptr(scales), scales.shape[1], _ptr(status),
+                                         _stream(stream)), "moe_quant_1x128_dispatch")
+    return q, scales
+
+
 def moe_quant_128x128(w: torch.Tensor, q: Optional[torch.Tensor] = None,
                       scales: Optional[torch.Tensor] = None, stream=None):
     """w float32 [R, C] -> (q uint8 [R, C], scales float32 [R/128, C/128])."""
@@ -145,6 +166,11 @@ def moe_quant_128x128(w: torch.Tensor, q: Optional[torch.Tensor] = None,
     return q, scales
 
 
+def route_workspace_bytes(T: int, E: int, d: int) -> int:
+    """moe_route's workspace: T*E float32 logits, then 3*E*d bfloat16 centroid pieces."""
+    return (4 * T * E + 255) // 256 * 256 + 6 * E * d
+
+
 def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
               ws: Optional[torch.Tensor] = None, out: Optional[dict] = None, stream=None) -> dict:
     _bits(u, torch.bfloat16)
@@ -158,7 +184,7 @@ def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: i
                "tie": torch.empty((T,), dtype=torch.uint8, device=dev),
                "counts": torch.empty((E,), dtype=torch.int32, device=dev)}
     if ws is None:
-        ws = torch.empty(max(4 * T * E, 256), dtype=torch.uint8, device=dev)
+        ws = torch.empty(route_workspace_bytes(T, E, d), dtype=torch.uint8, device=dev)
     _check(_lib.moe_route(_ptr(u), _ptr(centroids), _ptr(bias), T, d, E, K, _ptr(out["idx"]),
                           _ptr(out["gate"]), _ptr(out["tie"]), _ptr(out["counts"]), _ptr(ws),
                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")

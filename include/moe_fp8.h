@@ -100,6 +100,19 @@ size_t moe_workspace_size(const moe_layer_t* L, int T_max);
 int moe_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather_rows, int M, int d,
                     uint8_t* q, float* scales, int scale_ld, int32_t* status, void* stream);
 
+/* The dispatch-fused form of moe_quant_1x128 ([TH] Key ideas, FP8 bullet;
+ * [YLY] §4.3 and §2.2): quantisation is row-local, so every token is
+ * quantised once and its codes and scales are written to each row the
+ * dispatch gave it -- routed rows inv_row[t, 0..K) (moe_permute) and shared
+ * rows T*K + s*T + t, s < S.  Same rule and the same bits as
+ * moe_quant_1x128 with gather_rows = perm_token.
+ *   x [T, d] bf16; q [T*(K+S), d] fp8; scales at scales[kb * scale_ld + row],
+ *   scale_ld >= T*(K+S).  1 <= K + S <= 32.  A routed row outside
+ *   [0, T*(K+S)) is skipped and flagged MOE_ERR_BAD_INDEX in *status. */
+int moe_quant_1x128_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_row, int K,
+                             int S, uint8_t* q, float* scales, int scale_ld, int32_t* status,
+                             void* stream);
+
 /* 128x128 block quantisation of a weight matrix ([TH] Key ideas, FP8 bullet;
  * [YLY] §4.3), same rounding rule as moe_quant_1x128 with one scale per
  * block.  w [R, C] float32; q [R, C] fp8; scales [R/128, C/128].  R and C
@@ -116,7 +129,10 @@ int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, v
  *                          rounding), else 0,
  *   counts [E] int32       selections per expert (overwritten).
  * u [T, d] bf16; centroids [E, d]; bias [E].  1 <= K <= min(E, 32),
- * E <= 1024.  Workspace: at least T * E * 4 bytes, 256-byte aligned. */
+ * E <= 1024.  The logits run on the tensor cores: each float32 centroid is
+ * split exactly into three bfloat16 pieces and the products are summed in
+ * float32.  Workspace (256-byte aligned): T*E float32 logits, then, from the
+ * next 256-byte boundary, 3*E*d bfloat16 centroid pieces. */
 int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
               int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
               void* ws, size_t ws_bytes, void* stream);

@@ -163,3 +163,19 @@ def test_update_bias_bit_exact(L, orc):
     L.moe_update_bias(torch.from_numpy(counts).cuda(), bd, T, K, 1e-3)
     torch.cuda.synchronize()
     assert np.array_equal(bd.cpu().numpy(), orc.update_bias(counts, b.numpy(), T, K, 1e-3))
+
+
+@pytest.mark.parametrize("T,K,S,E,d", [(1, 1, 1, 4, 128), (97, 3, 2, 16, 384), (300, 8, 1, 64, 2048)])
+def test_quant_dispatch_bit_exact(L, orc, T, K, S, E, d):
+    rng = np.random.default_rng(T + d)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    o = orc.dispatch(idx, E)
+    x = wl.normal(wl.stream_key(34, T, d), (T, d), 1.5)
+    x[0, :128] = 0.0
+    xb = x.to(torch.bfloat16)
+    q, s = L.moe_quant_1x128_dispatch(xb.cuda(), torch.from_numpy(o["inv_row"]).cuda(), K, S)
+    torch.cuda.synchronize()
+    qt, st = orc.quant_1x128(bits(xb))                # each token quantised once
+    rows = np.concatenate([o["perm_token"], np.tile(np.arange(T), S)])
+    assert np.array_equal(q.cpu().numpy(), qt[rows])
+    assert np.array_equal(s.cpu().numpy(), st[rows].T)
