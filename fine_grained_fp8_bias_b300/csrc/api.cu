@@ -15,7 +15,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Workspace layout shared by moe_forward, moe_route and moe_permute.
 struct Layout {
-    size_t status, logits, csplit, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
+    size_t status, logits, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
 };
 
 Layout layout(int T, int d, int E, int K, int S, int I) {
@@ -30,7 +30,6 @@ Layout layout(int T, int d, int E, int K, int S, int I) {
     const size_t nchunks = ((size_t)T + kPermuteChunk - 1) / kPermuteChunk;
     L.status = take(16);
     L.logits = take(sizeof(float) * (size_t)T * E);
-    L.csplit = take(sizeof(uint16_t) * 3 * (size_t)E * d);
     L.hist = take(sizeof(int32_t) * nchunks * E);
     L.base = take(sizeof(int32_t) * nchunks * E);
     L.go = take(sizeof(int32_t) * (size_t)(E + S + 1));
@@ -62,10 +61,6 @@ int check_layer(const moe_layer_t* L) {
 }
 
 inline cudaStream_t S_(void* s) { return static_cast<cudaStream_t>(s); }
-
-// moe_route's workspace: T*E float32 logits, then (256-byte aligned) the
-// 3*E*d bfloat16 centroid pieces.
-size_t route_split_offset(int T, int E) { return align_up(sizeof(float) * (size_t)T * E, 256); }
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -152,13 +147,10 @@ int moe_route(const uint16_t* u, const float* centroids, const float* bias, int 
     if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!counts || !centroids || !bias) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!u || !topk_idx || !topk_gate || !tie_flag || !ws)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_MISALIGNED;
-    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
-    const size_t split_at = route_split_offset(T, E);
-    if (ws_bytes < split_at + sizeof(uint16_t) * 3 * (size_t)E * d) return MOE_ERR_WORKSPACE;
+    if (!aligned16(u) || !aligned16(centroids) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < sizeof(float) * (size_t)T * E) return MOE_ERR_WORKSPACE;
     return launch_route(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
-                        static_cast<float*>(ws), S_(stream),
-                        reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + split_at));
+                        static_cast<float*>(ws), S_(stream));
 }
 
 int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* offsets,
@@ -229,7 +221,6 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     const cudaStream_t st = S_(stream);
     int32_t* status = reinterpret_cast<int32_t*>(base + W.status);
     float* logits = reinterpret_cast<float*>(base + W.logits);
-    uint16_t* csplit = reinterpret_cast<uint16_t*>(base + W.csplit);
     int32_t* hist = reinterpret_cast<int32_t*>(base + W.hist);
     int32_t* bbase = reinterpret_cast<int32_t*>(base + W.base);
     int32_t* go = reinterpret_cast<int32_t*>(base + W.go);
@@ -246,7 +237,7 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
     if (e != cudaSuccess) return cuda_fail(e);
     if ((rc = launch_route(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
-                           counts, logits, st, csplit, status)))
+                           counts, logits, st)))
         return rc;
     if (T == 0) return MOE_OK;
     if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,

@@ -52,11 +52,9 @@ int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_ro
                           uint8_t* q, float* scales, int scale_ld, int32_t* status,
                           cudaStream_t st);
 int launch_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, cudaStream_t st);
-// cent_split: workspace of 3 * E * d bf16 for the tensor-core logits, or
-// null for the float32 CUDA-core logits kernel.
 int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                  int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
-                 cudaStream_t st, uint16_t* cent_split = nullptr, int32_t* status = nullptr);
+                 cudaStream_t st);
 int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);

@@ -167,8 +167,8 @@ def moe_quant_128x128(w: torch.Tensor, q: Optional[torch.Tensor] = None,
 
 
 def route_workspace_bytes(T: int, E: int, d: int) -> int:
-    """moe_route's workspace: T*E float32 logits, then 3*E*d bfloat16 centroid pieces."""
-    return (4 * T * E + 255) // 256 * 256 + 6 * E * d
+    """moe_route's workspace: the T*E float32 logits."""
+    return max(4 * T * E, 256)
 
 
 def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,

@@ -129,10 +129,9 @@ int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, v
  *                          rounding), else 0,
  *   counts [E] int32       selections per expert (overwritten).
  * u [T, d] bf16; centroids [E, d]; bias [E].  1 <= K <= min(E, 32),
- * E <= 1024.  The logits run on the tensor cores: each float32 centroid is
- * split exactly into three bfloat16 pieces and the products are summed in
- * float32.  Workspace (256-byte aligned): T*E float32 logits, then, from the
- * next 256-byte boundary, 3*E*d bfloat16 centroid pieces. */
+ * E <= 1024.  Logits are float32 sums with compensation (error about one
+ * float32 rounding).  Workspace: at least T * E * 4 bytes (the logits),
+ * 16-byte aligned. */
 int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
               int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
               void* ws, size_t ws_bytes, void* stream);

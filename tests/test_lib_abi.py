@@ -57,8 +57,6 @@ def test_host_side_validation_needs_no_device(lib):
     assert L.moe_route(fake, fake, fake, 4, 128, 2048, 8, fake, fake, fake, fake, fake, 1 << 20, None) == -1
     # workspace too small, misaligned pointer
     assert L.moe_route(fake, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 16, None) == -6
-    # logits fit but not the bf16 centroid pieces
-    assert L.moe_route(fake, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 256 + 6 * 8 * 128 - 1, None) == -6
     assert L.moe_route(fake + 8, fake, fake, 4, 128, 8, 2, fake, fake, fake, fake, fake, 1 << 20, None) == -3
     assert L.moe_permute(fake, 4, 2, 8, 1, fake, None, fake, fake, None, fake, 0, None) == -6
     # GEMM: bad mode, N not a multiple of 128, too many groups, null pointers
