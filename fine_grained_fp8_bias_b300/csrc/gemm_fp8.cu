@@ -389,15 +389,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t tbase = tmem_base + lane_addr + (it & 1) * BN;
                 tmem_ld32_nowait(tbase + c0 + 32, b);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(a[i]), s_lo, acc[i]);
+                fma2_scale<32>(acc, a, s_lo);
                 tmem_ld_wait(b);
                 tmem_ld32_nowait(tbase + c1, a);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(__uint_as_float(b[i]), s_lo, acc[32 + i]);
+                fma2_scale<32>(acc + 32, b, s_lo);
                 tmem_ld_wait(a);
                 tmem_ld32_nowait(tbase + c1 + 32, b);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(__uint_as_float(a[i]), s_hi, acc[64 + i]);
+                fma2_scale<32>(acc + 64, a, s_hi);
                 tmem_ld_wait(b);
                 // the whole slab is in registers: hand the TMEM buffer back
                 tc_fence_before();
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld32_nowait(tmem_base + lane_addr + ((it + 1) & 1) * BN + c0, a);
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[96 + i] = fmaf(__uint_as_float(b[i]), last_hi, acc[96 + i]);
+                fma2_scale<32>(acc + 96, b, last_hi);
                 if (kb + 1 < KB) tmem_ld_wait(a);
             }
             if (!ok) break;

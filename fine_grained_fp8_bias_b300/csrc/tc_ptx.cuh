@@ -174,6 +174,24 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[3
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// acc[2i..2i+1] = fma(v[2i..2i+1], s, acc[..]) with the packed two-lane
+// float32 FMA of sm_100+ (two independent round-to-nearest FMAs: the same
+// bits as two fmaf calls, half the instructions).
+template <int N>
+__device__ __forceinline__ void fma2_scale(float* acc, const uint32_t* v, float s) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        asm("{\n\t.reg .b64 d, a, b;\n\t"
+            "mov.b64 d, {%0, %1};\n\t"
+            "mov.b64 a, {%2, %3};\n\t"
+            "mov.b64 b, {%4, %4};\n\t"
+            "fma.rn.f32x2 d, a, b, d;\n\t"
+            "mov.b64 {%0, %1}, d;\n\t}"
+            : "+f"(acc[i]), "+f"(acc[i + 1])
+            : "r"(v[i]), "r"(v[i + 1]), "f"(s));
+    }
+}
+
 // Wait for this thread's outstanding TMEM loads.  The registers pass through
 // the asm as read-write operands, so no use of them can move above the wait.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
