@@ -50,6 +50,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest replica's time for the timed region (all-reduce MAX; the
+    process group is NCCL on GPUs, gloo in the CPU tests)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, T: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every replica processed T tokens per step, and the
+    job took as long as its slowest replica."""
+    return world * T * steps / (ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -266,12 +282,9 @@ def run_ours(args, world, rank, local):
     counts = step.rout["counts"].cpu()
     touched = int((counts > 0).sum()) + cfg.S
     T = cfg.T
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, total_ms)
 
     # per-kernel roofline
     abytes = algorithmic_bytes(cfg, T, touched)
@@ -338,14 +351,10 @@ def run_e2e(layer, cfg, dev, steps, world):
         h_host.copy_(out["h"], non_blocking=True)
     e.record()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(s.elapsed_time(e), world, dev)
     if layer.status() != 0:
         raise RuntimeError("device status flagged in the end-to-end loop")
-    return {"value": round(world * cfg.T * steps / (ms / 1e3), 1), "unit": "tokens/s",
+    return {"value": round(job_tokens_per_s(world, cfg.T, steps, ms), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 4,
             "steps": steps, "ms_per_step": round(ms / steps, 4)}
 
