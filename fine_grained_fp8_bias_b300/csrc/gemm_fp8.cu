@@ -126,6 +126,25 @@ __device__ __forceinline__ Tile find_tile(const Ctl* ctl, int G, int tile) {
     return Tile{lo, local / mtiles, local % mtiles};
 }
 
+// x / scale for |x| <= 448 scale: with r = RN(1 / scale) and y = RN(x r), the
+// residual x - scale y is exact in one FMA, and RN(y + residual r) (one
+// Markstein correction step, 1990) gives the correctly rounded quotient
+// except in rare near-halfway cases, where it is one float32 ulp off; a
+// quotient that is exactly representable, such as an E4M3 tie point, is
+// always returned exactly.  The sum in the correction turns a -0 quotient
+// into +0, so the sign is taken from x (scale > 0).  The scale must be far
+// from underflow.
+__device__ __forceinline__ float div_rcp(float x, float scale, float r) {
+    const float y = x * r;
+    return copysignf(fmaf(fmaf(-scale, y, x), r, y), x);
+}
+__device__ __forceinline__ uint32_t quant4_rcp(float a, float b, float c, float d, float scale,
+                                               float r) {
+    const uint32_t lo = e4m3x2(div_rcp(a, scale, r), div_rcp(b, scale, r));
+    const uint32_t hi = e4m3x2(div_rcp(c, scale, r), div_rcp(d, scale, r));
+    return lo | (hi << 16);
+}
+
 // ---------------------------------------------------------------- kernel
 template <bool GATE_UP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -388,16 +407,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; ok && kb < KB; ++kb, ++it) {
                 const uint32_t tbase = tmem_base + lane_addr + (it & 1) * BN;
                 tmem_ld32_nowait(tbase + c0 + 32, b);
-#pragma unroll
-                fma2_scale<32>(acc, a, s_lo);
+fma2_scale<32>(acc, a, s_lo);
                 tmem_ld_wait(b);
                 tmem_ld32_nowait(tbase + c1, a);
-#pragma unroll
-                fma2_scale<32>(acc + 32, b, s_lo);
+fma2_scale<32>(acc + 32, b, s_lo);
                 tmem_ld_wait(a);
                 tmem_ld32_nowait(tbase + c1 + 32, b);
-#pragma unroll
-                fma2_scale<32>(acc + 64, a, s_hi);
+fma2_scale<32>(acc + 64, a, s_hi);
                 tmem_ld_wait(b);
                 // the whole slab is in registers: hand the TMEM buffer back
                 tc_fence_before();
@@ -413,8 +429,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     tmem_ld32_nowait(tmem_base + lane_addr + ((it + 1) & 1) * BN + c0, a);
                 }
-#pragma unroll
-                fma2_scale<32>(acc + 96, b, last_hi);
+fma2_scale<32>(acc + 96, b, last_hi);
                 if (kb + 1 < KB) tmem_ld_wait(a);
             }
             if (!ok) break;
@@ -439,6 +454,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status)) { ok = false; break; }
                 amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
                 const float scale = tile_scale(amax);
+                // a tile scale below 2^-100 (amax below ~2^-91) takes IEEE division
+                const bool fast_div = scale >= 0x1p-100f;
+                const float rs = __frcp_rn(scale);
                 if (valid) {
                     uint8_t* dst = static_cast<uint8_t*>(p.out) + (size_t)grow * p.N + tl.nt * 128 + wg * 64;
 #pragma unroll
@@ -446,11 +464,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         uint4 o;
                         if (amax == 0.0f) {
                             o = make_uint4(0u, 0u, 0u, 0u);
-                        } else {
+                        } else if (!fast_div) {
                             o.x = quant4(acc[j + 0], acc[j + 1], acc[j + 2], acc[j + 3], scale);
                             o.y = quant4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7], scale);
                             o.z = quant4(acc[j + 8], acc[j + 9], acc[j + 10], acc[j + 11], scale);
                             o.w = quant4(acc[j + 12], acc[j + 13], acc[j + 14], acc[j + 15], scale);
+                        } else {
+                            o.x = quant4_rcp(acc[j + 0], acc[j + 1], acc[j + 2], acc[j + 3], scale, rs);
+                            o.y = quant4_rcp(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7], scale, rs);
+                            o.z = quant4_rcp(acc[j + 8], acc[j + 9], acc[j + 10], acc[j + 11], scale, rs);
+                            o.w = quant4_rcp(acc[j + 12], acc[j + 13], acc[j + 14], acc[j + 15], scale, rs);
                         }
                         *reinterpret_cast<uint4*>(dst + j) = o;
                     }
