@@ -58,6 +58,7 @@ constexpr int EPI_WARP0 = 4;                    // first epilogue warp
 constexpr int NUM_THREADS = 128 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;             // 2 buffers x 256 fp32 columns
 constexpr int SCALE_SLOTS = 8;                  // depth of the scale ring
+constexpr int SCALE_LAG = 3;                    // copy groups in flight before a slab is published
 // Register split: the kernel is compiled for 384 threads x 168 registers
 // (64512); warpgroup 0 drops to 40 and the two epilogue warpgroups rise to
 // 232: 128 * 40 + 256 * 232 = 64512.  Per SM sub-partition (warps w, w+4,
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
             }
             for (int s = 0; s < SCALE_SLOTS; ++s) {
-                mbar_init(&ctl->sfull[s], 32);   // one asynchronous arrival per loader lane
+                mbar_init(&ctl->sfull[s], 32);   // one arrival per loader lane
                 mbar_init(&ctl->sempty[s], NUM_EPI_WARPS);
             }
             mbar_init(&ctl->xbar, NUM_EPI_WARPS);
@@ -325,9 +326,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, &ctl->abort, p.status);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
                 // 4-byte asynchronous copies; rows outside the group are zero-filled
-                // (source size 0).  Each lane's copies arrive on sfull when they land,
-                // so the loader never waits for global memory and runs up to
-                // SCALE_SLOTS slabs ahead.
+                // (source size 0).  One commit group per slab; slab it - SCALE_LAG is
+                // announced on its sfull barrier once its group has landed, so the
+                // loader runs up to SCALE_SLOTS slabs ahead and each slab is published
+                // as soon as its own copies are complete.  (An mbarrier arrive tied
+                // to cp.async completion would wait for every earlier copy of the
+                // thread, including the newer slabs' copies in flight.)
                 ScaleSlot& sl = ctl->scales[slot];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -342,12 +346,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     cp_async4(&sl.sw[0], w0 + kb, 4u);
                     cp_async4(&sl.sw[1], w1 + kb, 4u);
                 }
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
-                                 smem_u32(&ctl->sfull[slot]))
-                             : "memory");
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                if (it >= (uint32_t)SCALE_LAG) {
+                    asm volatile("cp.async.wait_group %0;" ::"n"(SCALE_LAG) : "memory");
+                    mbar_arrive(&ctl->sfull[(it - SCALE_LAG) % SCALE_SLOTS]);
+                }
             }
         }
+        // publish the slabs still in flight (on abort nobody waits for them)
         asm volatile("cp.async.wait_all;" ::: "memory");
+        if (ok)
+            for (uint32_t j = it > (uint32_t)SCALE_LAG ? it - SCALE_LAG : 0; j < it; ++j)
+                mbar_arrive(&ctl->sfull[j % SCALE_SLOTS]);
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
@@ -394,7 +404,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
                 return true;
             };
-            if (KB > 0) {
+            // A warp whose 32 rows all lie past the group's last row (the padding
+            // of a group's last tile) keeps the barrier protocol but neither
+            // reads TMEM nor promotes.
+            const bool warp_active = tl.mt * BM + quarter * 32 < m_g;
+            if (!warp_active) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    float lo, hi;
+                    if (!take_scales(it, lo, hi) ||
+                        !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->tempty[it & 1]);
+                }
+            } else if (KB > 0) {
                 if (!take_scales(it, s_lo, s_hi) ||
                     !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status)) {
                     ok = false;
@@ -404,16 +429,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld_wait(a);
                 }
             }
-            for (int kb = 0; ok && kb < KB; ++kb, ++it) {
+            for (int kb = 0; ok && warp_active && kb < KB; ++kb, ++it) {
                 const uint32_t tbase = tmem_base + lane_addr + (it & 1) * BN;
                 tmem_ld32_nowait(tbase + c0 + 32, b);
-fma2_scale<32>(acc, a, s_lo);
+                fma2_scale<32>(acc, a, s_lo);
                 tmem_ld_wait(b);
                 tmem_ld32_nowait(tbase + c1, a);
-fma2_scale<32>(acc + 32, b, s_lo);
+                fma2_scale<32>(acc + 32, b, s_lo);
                 tmem_ld_wait(a);
                 tmem_ld32_nowait(tbase + c1 + 32, b);
-fma2_scale<32>(acc + 64, a, s_hi);
+                fma2_scale<32>(acc + 64, a, s_hi);
                 tmem_ld_wait(b);
                 // the whole slab is in registers: hand the TMEM buffer back
                 tc_fence_before();
@@ -429,19 +454,22 @@ fma2_scale<32>(acc + 64, a, s_hi);
                     tc_fence_after();
                     tmem_ld32_nowait(tmem_base + lane_addr + ((it + 1) & 1) * BN + c0, a);
                 }
-fma2_scale<32>(acc + 96, b, last_hi);
+                fma2_scale<32>(acc + 96, b, last_hi);
                 if (kb + 1 < KB) tmem_ld_wait(a);
             }
             if (!ok) break;
             // ---- tile finalisation
             if constexpr (gate_up) {
                 float amax = 0.0f;
+                if (warp_active) {
+                    // h = SiLU(g) * u with SiLU(g) = g / (1 + e^-g)
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float gv = acc[i];
-                    const float h = __fdiv_rn(gv, 1.0f + expf(-gv)) * acc[64 + i];
-                    acc[i] = h;
-                    amax = fmaxf(amax, fabsf(h));
+                    for (int i = 0; i < 64; ++i) {
+                        const float gv = acc[i];
+                        const float h = __fdiv_rn(gv, 1.0f + expf(-gv)) * acc[64 + i];
+                        acc[i] = h;
+                        amax = fmaxf(amax, fabsf(h));
+                    }
                 }
                 // Exchange the row's amax with the other warpgroup.  One xbar phase per
                 // tile: no warp can arrive for tile n+1 before all arrived for tile n,
