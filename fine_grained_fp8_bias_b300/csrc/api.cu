@@ -15,7 +15,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Workspace layout shared by moe_forward, moe_route and moe_permute.
 struct Layout {
-    size_t status, logits, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
+    size_t status, route, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
 };
 
 Layout layout(int T, int d, int E, int K, int S, int I) {
@@ -29,7 +29,7 @@ Layout layout(int T, int d, int E, int K, int S, int I) {
     const size_t M = (size_t)T * (K + S);
     const size_t nchunks = ((size_t)T + kPermuteChunk - 1) / kPermuteChunk;
     L.status = take(16);
-    L.logits = take(sizeof(float) * (size_t)T * E);
+    L.route = take(route_ws_bytes(T, d, E));
     L.hist = take(sizeof(int32_t) * nchunks * E);
     L.base = take(sizeof(int32_t) * nchunks * E);
     L.go = take(sizeof(int32_t) * (size_t)(E + S + 1));
@@ -139,6 +139,27 @@ int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, v
     return launch_quant_128x128(w, R, C, q, scales, S_(stream));
 }
 
+size_t moe_route_workspace_size(int T, int d, int E) {
+    if (T < 0 || d <= 0 || E <= 0 || d % 128 || E > kMaxExperts) return 0;
+    return route_ws_bytes(T, d, E);
+}
+
+int moe_route_estimate_logits(const uint16_t* u, const float* centroids, int T, int d, int E,
+                              float* logits, float* cmax, void* ws, size_t ws_bytes,
+                              void* stream) {
+    if (T < 0 || d <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!u || !centroids || !logits || !cmax || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < route_ws_bytes(T, d, E)) return MOE_ERR_WORKSPACE;
+    int32_t* status = static_cast<int32_t*>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), S_(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_route_estimate(u, centroids, T, d, E, logits, cmax, ws, status, S_(stream));
+}
+
 int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
               int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
               void* ws, size_t ws_bytes, void* stream) {
@@ -147,10 +168,17 @@ int moe_route(const uint16_t* u, const float* centroids, const float* bias, int 
     if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!counts || !centroids || !bias) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!u || !topk_idx || !topk_gate || !tie_flag || !ws)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(u) || !aligned16(centroids) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
-    if (ws_bytes < sizeof(float) * (size_t)T * E) return MOE_ERR_WORKSPACE;
-    return launch_route(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
-                        static_cast<float*>(ws), S_(stream));
+    if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_MISALIGNED;
+    if (T == 0) return launch_route_tc(u, centroids, bias, 0, d, E, K, topk_idx, topk_gate,
+                                       tie_flag, counts, ws, nullptr, S_(stream));
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < route_ws_bytes(T, d, E)) return MOE_ERR_WORKSPACE;
+    // the workspace's first int32 is the status word of this call
+    int32_t* status = static_cast<int32_t*>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), S_(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_route_tc(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
+                           ws, status, S_(stream));
 }
 
 int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* offsets,
@@ -220,7 +248,7 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     char* base = static_cast<char*>(ws);
     const cudaStream_t st = S_(stream);
     int32_t* status = reinterpret_cast<int32_t*>(base + W.status);
-    float* logits = reinterpret_cast<float*>(base + W.logits);
+    void* route_ws = base + W.route;
     int32_t* hist = reinterpret_cast<int32_t*>(base + W.hist);
     int32_t* bbase = reinterpret_cast<int32_t*>(base + W.base);
     int32_t* go = reinterpret_cast<int32_t*>(base + W.go);
@@ -236,8 +264,8 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
 
     cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
     if (e != cudaSuccess) return cuda_fail(e);
-    if ((rc = launch_route(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
-                           counts, logits, st)))
+    if ((rc = launch_route_tc(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
+                              counts, route_ws, status, st)))
         return rc;
     if (T == 0) return MOE_OK;
     if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,

@@ -55,6 +55,17 @@ int launch_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales
 int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                  int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
                  cudaStream_t st);
+// The tensor-core router of moe_route (route_tc.cu): workspace bytes for T
+// tokens, and the launch (the workspace's first int32 is not touched; the
+// status word is passed separately).
+size_t route_ws_bytes(int T, int d, int E);
+int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
+                    int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
+                    int32_t* status, cudaStream_t st);
+// The router's logit estimates summed into out [T, E], and the bound's
+// largest centroid norm into *cmax_out (device), for checking the bound.
+int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,
+                          float* cmax_out, void* ws, int32_t* status, cudaStream_t st);
 int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);

@@ -1,0 +1,545 @@
+// Router of moe_route: affinity, sigmoid, bias-steered top-K and gates, with
+// the logits screened on the tensor cores and recomputed exactly only where
+// the selection depends on them.
+//
+// Source: "รายงานเชิงเทคนิคของ DeepSeek-V3" (xyznot.com/th/paper/2412.19437),
+// Method §2: s_{i,t} = Sigmoid(u_t^T e_i); expert i is selected for token t
+// when s_{i,t} + b_i is among the K_r largest of {s_{j,t} + b_j}; the gates
+// are the selected s normalised to sum 1.  "Deepseek V3 国货之光 开源之光"
+// (databean.com.cn), "Auxiliary-Loss-Free Load Balancing": b only steers the
+// choice, the gates use the unbiased s.
+//
+// The selection has a near-tie band 1e-6 wide, so the scores it compares must
+// be close to exact; only about K of the E logits of a token matter, though.
+//   1. split_centroids: c = hi + mid + r with hi = bf16(c), mid = bf16(c - hi)
+//      (|r| <= 2^-16 |c| elementwise), and the largest centroid norm.
+//   2. logits_tc: l~ = u hi^T + u mid^T on the tensor cores
+//      (tcgen05.mma.kind::f16, bf16 operands, float32 accumulation in TMEM),
+//      split over d when there are few token tiles; partial sums to [split][T][E].
+//   3. select_refine, one warp per token: the approximate biased scores
+//      z~ = sigmoid(l~) + b give the K-th largest z~_K.  |l~ - l| is bounded by
+//      gamma |u_t| max_e |c_e| (gamma = 2^-11 covers the split remainder and an
+//      error of one float32 ulp of the running sum per MMA instruction, with
+//      twofold headroom), and sigmoid has slope at most 1/4, which bounds
+//      |z~ - z| by eps.  Every expert with z~ >= z~_K - 2 eps - 2e-6 is a
+//      candidate: no other expert can be selected or lie within 2e-6 of the
+//      K-th score.  The candidates' logits are recomputed on CUDA cores with
+//      compensated summation (32-term FMA chains added with TwoSum), and the
+//      selection, gates and tie flag use those.  A token with more than 32
+//      candidates (degenerate inputs: many equal scores) recomputes all E.
+// Selection order: descending s + b, equal scores broken by the lower expert
+// index.  Near-tie flag: the K-th and (K+1)-th biased scores differ by less
+// than 1e-6.
+#include <cfloat>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+using namespace tc;
+
+constexpr int RT_M = 128;                           // tokens per tile
+constexpr int RT_N = 128;                           // experts per tile
+constexpr int RT_K = 64;                            // bf16 elements per slab (128 bytes)
+constexpr int RT_STAGES = 4;
+constexpr int RT_SMEM_A = RT_M * RT_K * 2;          // 16 KB
+constexpr int RT_SMEM_B = RT_N * RT_K * 2;          // 16 KB per centroid piece
+constexpr int RT_STAGE = RT_SMEM_A + 2 * RT_SMEM_B; // 48 KB
+constexpr int RT_THREADS = 128;
+constexpr uint32_t RT_TMEM_COLS = 128;
+constexpr int CAND_CAP = 32;
+constexpr float GAMMA = 0x1p-11f;
+constexpr int SEL_WARPS = 4;                        // tokens per select_refine block
+
+struct RtCtl {
+    uint64_t full[RT_STAGES];
+    uint64_t empty[RT_STAGES];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t RT_SMEM_BYTES = 1024 + (size_t)RT_STAGES * RT_STAGE + sizeof(RtCtl);
+
+// Workspace: header (status word, largest centroid norm), hi, mid, partial logits.
+struct RouteWs {
+    size_t status, cmax, hi, mid, part, total;
+    int split;
+};
+
+int route_split(int T, int E, int d) {
+    const int tiles = ((T + RT_M - 1) / RT_M) * ((E + RT_N - 1) / RT_N);
+    const int slabs = d / RT_K;
+    int split = 1;
+    while (tiles * split * 2 <= 148 && split * 2 <= slabs / 8) split *= 2;
+    return split;
+}
+
+RouteWs route_ws(int T, int d, int E) {
+    RouteWs w{};
+    w.split = route_split(T, E, d);
+    w.status = 0;
+    w.cmax = 16;
+    w.hi = 256;
+    w.mid = align_up(w.hi + (size_t)E * d * 2, 256);
+    w.part = align_up(w.mid + (size_t)E * d * 2, 256);
+    w.total = align_up(w.part + sizeof(float) * (size_t)w.split * T * E, 256);
+    return w;
+}
+
+// Error-free sum (Knuth's TwoSum): s + err == a + b exactly.
+__device__ __forceinline__ float two_sum(float a, float b, float& err) {
+    const float s = a + b;
+    const float bb = s - a;
+    err = (a - (s - bb)) + (b - bb);
+    return s;
+}
+
+__device__ __forceinline__ float sigmoid(float x) { return __fdiv_rn(1.0f, 1.0f + expf(-x)); }
+
+// Larger score first; equal scores: lower expert index first.
+__device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
+    return za > zb || (za == zb && ia < ib);
+}
+
+// ------------------------------------------------------------ 1. split
+// One warp per expert row: hi/mid pieces and |c_e|; the largest norm (times
+// 1 + 2^-20 for its own rounding) goes to *cmax_bits with an integer max,
+// which orders non-negative floats correctly.
+__global__ void __launch_bounds__(256) split_centroids_kernel(const float* __restrict__ c, int E,
+                                                              int d, uint16_t* __restrict__ hi,
+                                                              uint16_t* __restrict__ mid,
+                                                              unsigned int* __restrict__ cmax_bits) {
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); e < E; e += nw) {
+        float ss = 0.0f;
+        for (int j = lane * 4; j < d; j += 128) {
+            const size_t at = (size_t)e * d + j;
+            const float4 v = *reinterpret_cast<const float4*>(c + at);
+            const float x[4] = {v.x, v.y, v.z, v.w};
+            uint16_t h[4], m[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat16 bh = __float2bfloat16_rn(x[i]);
+                const __nv_bfloat16 bm = __float2bfloat16_rn(x[i] - __bfloat162float(bh));
+                h[i] = __bfloat16_as_ushort(bh);
+                m[i] = __bfloat16_as_ushort(bm);
+                ss = fmaf(x[i], x[i], ss);
+            }
+            *reinterpret_cast<uint2*>(hi + at) =
+                make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+            *reinterpret_cast<uint2*>(mid + at) =
+                make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) atomicMax(cmax_bits, __float_as_uint(sqrtf(ss) * (1.0f + 0x1p-20f)));
+    }
+}
+
+// ------------------------------------------------------------ 2. logits_tc
+// One CTA: 128 tokens x 128 experts over the slabs [kb0, kb1) of d.  Warp 0
+// lane 0 loads (TMA, 128-byte swizzle), warp 1 lane 0 issues the MMAs (both
+// pieces into one TMEM accumulator), then all four warps read TMEM (thread
+// (warp, lane) owns token row 32 warp + lane) and store the partial sums.
+__global__ void __launch_bounds__(RT_THREADS, 1)
+    logits_tc_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
+                     const __grid_constant__ CUtensorMap tmM, int T, int d, int E, int split,
+                     float* __restrict__ part, int32_t* status) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    RtCtl* ctl = reinterpret_cast<RtCtl*>(smem + (size_t)RT_STAGES * RT_STAGE);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * RT_M, e0 = blockIdx.y * RT_N;
+    const int slabs = d / RT_K;
+    const int kb0 = (int)((long long)slabs * blockIdx.z / split);
+    const int kb1 = (int)((long long)slabs * (blockIdx.z + 1) / split);
+
+    if (warp == 0 && lane == 0) {
+        ctl->abort = 0;
+        for (int s = 0; s < RT_STAGES; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmU);
+        tma_prefetch_desc(&tmH);
+        tma_prefetch_desc(&tmM);
+    } else if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&ctl->tmem_base)),
+                     "r"(RT_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % RT_STAGES;
+                if (!mbar_wait(&ctl->empty[s], ((it / RT_STAGES) & 1) ^ 1, &ctl->abort, status)) break;
+                uint8_t* sA = smem + (size_t)s * RT_STAGE;
+                mbar_expect_tx(&ctl->full[s], RT_STAGE);
+                tma_load_2d(sA, &tmU, &ctl->full[s], kb * RT_K, t0);
+                tma_load_2d(sA + RT_SMEM_A, &tmH, &ctl->full[s], kb * RT_K, e0);
+                tma_load_2d(sA + RT_SMEM_A + RT_SMEM_B, &tmM, &ctl->full[s], kb * RT_K, e0);
+            }
+            // no copy may still be landing when the CTA exits
+            const uint32_t first = it > (uint32_t)RT_STAGES ? it - RT_STAGES : 0;
+            for (uint32_t j = first; j < it; ++j) mbar_drain(&ctl->full[j % RT_STAGES], (j / RT_STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(RT_M, RT_N);
+            uint32_t it = 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % RT_STAGES;
+                if (!mbar_wait(&ctl->full[s], (it / RT_STAGES) & 1, &ctl->abort, status)) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smem + (size_t)s * RT_STAGE);
+                const uint32_t bh = a0 + RT_SMEM_A, bm = bh + RT_SMEM_B;
+#pragma unroll
+                for (int k = 0; k < RT_K / 16; ++k)
+                    mma_bf16(tmem_base, sdesc_sw128(a0 + k * 32), sdesc_sw128(bh + k * 32), idesc,
+                             (kb > kb0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < RT_K / 16; ++k)
+                    mma_bf16(tmem_base, sdesc_sw128(a0 + k * 32), sdesc_sw128(bm + k * 32), idesc, 1u);
+                mma_commit(&ctl->empty[s]);
+            }
+            // committed in every case, so the epilogue and the teardown can wait
+            // for the MMAs in flight
+            mma_commit(&ctl->done);
+        }
+    }
+    __syncwarp();
+    // epilogue: every warp, after the accumulator is complete
+    if (warp_wait(&ctl->done, 0, &ctl->abort, status)) {
+        tc_fence_after();
+        const int t = t0 + warp * 32 + lane;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        float* dst = part + ((size_t)blockIdx.z * T + (t < T ? t : 0)) * E;
+#pragma unroll
+        for (int c = 0; c < RT_N / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32_nowait(taddr + c * 32, v);
+            tmem_ld_wait(v);
+            if (t < T) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int e = e0 + c * 32 + i;
+                    if (e < E) dst[e] = __uint_as_float(v[i]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        if (lane == 0) mbar_drain(&ctl->done, 0);
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(RT_TMEM_COLS));
+    }
+}
+
+// ------------------------------------------------------------ 3. select_refine
+// l = u_t . c_e with compensated summation.  Lane L takes elements
+// 128 i + 4 L .. + 3; each 32-product FMA chain starts from zero and is added
+// into (acc, cmp) with TwoSum; the lanes' pairs are then combined with TwoSum
+// too (the xor butterfly leaves the same value in every lane).
+__device__ __forceinline__ float exact_dot(const uint16_t* ut, const float* __restrict__ crow,
+                                           int d, int lane) {
+    float acc = 0.0f, cmp = 0.0f;
+    const int nblk = d / 128;
+    for (int i = 0; i < nblk; i += 8) {
+        float4 cv[8];
+        uint2 uv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (i + q < nblk) {
+                const int j = (i + q) * 128 + lane * 4;
+                cv[q] = __ldg(reinterpret_cast<const float4*>(crow + j));
+                uv[q] = *reinterpret_cast<const uint2*>(ut + j);
+            }
+        }
+        float p = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (i + q < nblk) {
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].x & 0xFFFFu)), cv[q].x, p);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].x >> 16)), cv[q].y, p);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].y & 0xFFFFu)), cv[q].z, p);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].y >> 16)), cv[q].w, p);
+            }
+        }
+        float err;
+        acc = two_sum(acc, p, err);
+        cmp += err;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float oa = __shfl_xor_sync(0xffffffffu, acc, off);
+        const float oc = __shfl_xor_sync(0xffffffffu, cmp, off);
+        float err;
+        acc = two_sum(acc, oa, err);
+        cmp = (cmp + oc) + err;
+    }
+    return acc + cmp;
+}
+
+// The K-th largest value of z over the warp (lane L holds experts L + 32 j).
+template <int NV>
+__device__ __forceinline__ float kth_largest(const float (&z)[NV], int E, int K, int lane) {
+    unsigned taken = 0;
+    float zk = -FLT_MAX;
+    for (int k = 0; k < K; ++k) {
+        float bz = -FLT_MAX;
+        int be = 0x7fffffff, bj = -1;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if (e < E && !(taken >> j & 1u) && better(z[j], e, bz, be)) { bz = z[j]; be = e; bj = j; }
+        }
+        float wz = bz;
+        int we = be;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, wz, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, we, off);
+            if (better(oz, oe, wz, we)) { wz = oz; we = oe; }
+        }
+        if (we == be && bj >= 0) taken |= 1u << bj;
+        zk = wz;
+    }
+    return zk;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
+    const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
+    const float* __restrict__ part, int split, int T, int d, int E, int K,
+    const unsigned int* __restrict__ cmax_bits, int32_t* __restrict__ idx, float* __restrict__ gate,
+    uint8_t* __restrict__ tie, int32_t* __restrict__ counts) {
+    extern __shared__ __align__(16) uint16_t u_sm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * SEL_WARPS + warp;
+    if (t >= T) return;
+    uint16_t* ut = u_sm + (size_t)warp * d;
+    // token row to shared memory, and |u_t|^2
+    float ss = 0.0f;
+    for (int j = lane * 8; j < d; j += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(u + (size_t)t * d + j);
+        *reinterpret_cast<uint4*>(ut + j) = v;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
+            const float hi = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    __syncwarp();
+
+    // approximate biased scores and the candidate band
+    float za[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int e = j * 32 + lane;
+        if (e < E) {
+            float l = 0.0f;
+            for (int s = 0; s < split; ++s) l += part[((size_t)s * T + t) * E + e];
+            za[j] = sigmoid(l) + bias[e];
+        } else {
+            za[j] = -FLT_MAX;
+        }
+    }
+    const float zk_approx = kth_largest(za, E, K, lane);
+    const float eps_l = GAMMA * sqrtf(ss) * __uint_as_float(*cmax_bits);
+    const float eps_z = 0.25f * eps_l + 1e-6f + 0x1p-22f * (fabsf(zk_approx) + 1.0f);
+    const float thr = zk_approx - 2.0f * eps_z - 2e-6f;
+    unsigned cand = 0;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+        if (j * 32 + lane < E && za[j] >= thr) cand |= 1u << j;
+    int n = __popc(cand);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    if (n > CAND_CAP) {
+        cand = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            if (j * 32 + lane < E) cand |= 1u << j;
+    }
+
+    // exact scores of the candidates
+    float s[NV], z[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        s[j] = 0.0f;
+        z[j] = -FLT_MAX;
+        unsigned m = __ballot_sync(0xffffffffu, (cand >> j) & 1u);
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int e = j * 32 + src;
+            const float l = exact_dot(ut, c + (size_t)e * d, d, lane);
+            if (lane == src) {
+                s[j] = sigmoid(l);
+                z[j] = s[j] + bias[e];
+            }
+        }
+    }
+
+    // selection over the candidates (the others score -FLT_MAX)
+    unsigned taken = 0;
+    float my_s = 0.0f, ssum = 0.0f, zk = 0.0f, zk1 = -FLT_MAX;
+    int my_e = -1;
+    const int rounds = K < E ? K + 1 : K;
+    for (int k = 0; k < rounds; ++k) {
+        float bz = -FLT_MAX;
+        int be = 0x7fffffff, bj = -1;
+        float bs = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if ((cand >> j & 1u) && !(taken >> j & 1u) && better(z[j], e, bz, be)) {
+                bz = z[j]; be = e; bj = j; bs = s[j];
+            }
+        }
+        float wz = bz, ws = bs;
+        int we = be;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, wz, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, we, off);
+            const float os = __shfl_xor_sync(0xffffffffu, ws, off);
+            if (better(oz, oe, wz, we)) { wz = oz; we = oe; ws = os; }
+        }
+        if (we == be && bj >= 0) taken |= 1u << bj;
+        if (k < K) {
+            ssum += ws;                                  // same order in every lane
+            if (lane == k) { my_e = we; my_s = ws; }
+            if (k == K - 1) zk = wz;
+        } else {
+            zk1 = wz;                                    // -FLT_MAX: no candidate left
+        }
+    }
+    if (lane < K) {
+        idx[(size_t)t * K + lane] = my_e;
+        gate[(size_t)t * K + lane] = __fdiv_rn(my_s, ssum);
+        atomicAdd(&counts[my_e], 1);
+    }
+    if (lane == 0) tie[t] = (K < E && (zk - zk1) < 1e-6f) ? 1 : 0;
+}
+
+template <int NV>
+int launch_select(const uint16_t* u, const float* c, const float* bias, const float* part,
+                  int split, int T, int d, int E, int K, const unsigned int* cmax, int32_t* idx,
+                  float* gate, uint8_t* tie, int32_t* counts, cudaStream_t st) {
+    const size_t smem = (size_t)SEL_WARPS * d * sizeof(uint16_t);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(select_refine_kernel<NV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    select_refine_kernel<NV><<<(T + SEL_WARPS - 1) / SEL_WARPS, SEL_WARPS * 32, smem, st>>>(
+        u, c, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts);
+    return check_launch();
+}
+
+__global__ void sum_partials_kernel(const float* __restrict__ part, int split, size_t n,
+                                    float* __restrict__ out) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float v = 0.0f;
+        for (int s = 0; s < split; ++s) v += part[s * n + i];
+        out[i] = v;
+    }
+}
+
+// Steps 1 and 2 of the router; returns the partial-sum array.
+int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, void* ws,
+                    int32_t* status, cudaStream_t st, const float** part_out, int* split_out,
+                    const unsigned int** cmax_out) {
+    const RouteWs W = route_ws(T, d, E);
+    char* base = static_cast<char*>(ws);
+    unsigned int* cmax = reinterpret_cast<unsigned int*>(base + W.cmax);
+    uint16_t* hi = reinterpret_cast<uint16_t*>(base + W.hi);
+    uint16_t* mid = reinterpret_cast<uint16_t*>(base + W.mid);
+    float* part = reinterpret_cast<float*>(base + W.part);
+    cudaError_t e = cudaMemsetAsync(cmax, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int rc;
+    split_centroids_kernel<<<(E + 7) / 8, 256, 0, st>>>(cent, E, d, hi, mid, cmax);
+    if ((rc = check_launch())) return rc;
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)RT_SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        attr_set = true;
+    }
+    CUtensorMap mU, mH, mM;
+    if ((rc = make_map_2d(&mU, u, (uint64_t)T, (uint64_t)d, 2, RT_M, RT_K))) return rc;
+    if ((rc = make_map_2d(&mH, hi, (uint64_t)E, (uint64_t)d, 2, RT_N, RT_K))) return rc;
+    if ((rc = make_map_2d(&mM, mid, (uint64_t)E, (uint64_t)d, 2, RT_N, RT_K))) return rc;
+    const dim3 grid((T + RT_M - 1) / RT_M, (E + RT_N - 1) / RT_N, W.split);
+    logits_tc_kernel<<<grid, RT_THREADS, RT_SMEM_BYTES, st>>>(mU, mH, mM, T, d, E, W.split, part,
+                                                              status);
+    if ((rc = check_launch())) return rc;
+    *part_out = part;
+    *split_out = W.split;
+    *cmax_out = cmax;
+    return MOE_OK;
+}
+
+}  // namespace
+
+size_t route_ws_bytes(int T, int d, int E) { return route_ws(T, d, E).total; }
+
+int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,
+                          float* cmax_out, void* ws, int32_t* status, cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    const float* part;
+    const unsigned int* cmax;
+    int split, rc;
+    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &cmax))) return rc;
+    const size_t n = (size_t)T * E;
+    sum_partials_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(
+        part, split, n, out);
+    if ((rc = check_launch())) return rc;
+    const cudaError_t e = cudaMemcpyAsync(cmax_out, cmax, sizeof(float), cudaMemcpyDeviceToDevice, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
+                    int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
+                    int32_t* status, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (T == 0) return MOE_OK;
+    const float* part;
+    const unsigned int* cmax;
+    int split, rc;
+    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &cmax))) return rc;
+    const int nv = (E + 31) / 32;
+    if (nv <= 1) return launch_select<1>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+    if (nv <= 2) return launch_select<2>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+    if (nv <= 4) return launch_select<4>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+    if (nv <= 8) return launch_select<8>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+    if (nv <= 16) return launch_select<16>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+    return launch_select<32>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+}
+
+}  // namespace moe

@@ -48,13 +48,22 @@ def _load() -> ctypes.CDLL:
     lib.moe_status_string.argtypes = [I32]
     lib.moe_last_cuda_error.restype = I32
     lib.moe_kernel_launches.restype = ctypes.c_uint64
+    lib.moe_kernel_launches.argtypes = []
+    lib.moe_last_cuda_error.argtypes = []
     lib.moe_workspace_size.restype = ctypes.c_size_t
     lib.moe_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
+    lib.moe_route_workspace_size.restype = ctypes.c_size_t
+    lib.moe_route_workspace_size.argtypes = [I32, I32, I32]
+    # Every other entry point returns an int status.  Each one is called only
+    # with these argument types: ctypes would otherwise pass Python ints as C
+    # int and cut 64-bit pointers to 32 bits.
     sigs = {
         "moe_quant_1x128": [P, I32, P, I32, I32, P, P, I32, P, P],
         "moe_quant_128x128": [P, I32, I32, P, P, P],
         "moe_quant_1x128_dispatch": [P, I32, I32, P, I32, I32, P, P, I32, P, P],
         "moe_route": [P, P, P, I32, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
+        "moe_route_noalloc": [P, P, P, I32, I32, I32, I32, P, P, P, P, P],
+        "moe_route_estimate_logits": [P, P, I32, I32, I32, P, P, P, ctypes.c_size_t, P],
         "moe_permute": [P, I32, I32, I32, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_grouped_gemm_fp8": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
         "moe_combine": [P, P, P, P, P, I32, I32, I32, I32, P, P],
@@ -167,8 +176,8 @@ def moe_quant_128x128(w: torch.Tensor, q: Optional[torch.Tensor] = None,
 
 
 def route_workspace_bytes(T: int, E: int, d: int) -> int:
-    """moe_route's workspace: the T*E float32 logits."""
-    return max(4 * T * E, 256)
+    """moe_route's workspace bytes (moe_route_workspace_size)."""
+    return max(int(_lib.moe_route_workspace_size(T, d, E)), 256)
 
 
 def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
@@ -191,13 +200,27 @@ def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: i
     return out
 
 
+def moe_route_estimate_logits(u: torch.Tensor, centroids: torch.Tensor, stream=None):
+    """The router's tensor-core logit estimates [T, E] and the largest centroid
+    norm of its error bound (check hook of moe_route's screening step)."""
+    _bits(u, torch.bfloat16)
+    _dev(u, "u")
+    T, d = u.shape
+    E = centroids.shape[0]
+    out = torch.empty((T, E), dtype=torch.float32, device=u.device)
+    cmax = torch.empty((1,), dtype=torch.float32, device=u.device)
+    ws = torch.empty(route_workspace_bytes(T, E, d), dtype=torch.uint8, device=u.device)
+    _check(_lib.moe_route_estimate_logits(_ptr(u), _ptr(centroids), T, d, E, _ptr(out), _ptr(cmax),
+                                          _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_route_estimate_logits")
+    return out, cmax
+
+
 def moe_route_noalloc(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
                       out: Optional[dict] = None, stream=None) -> dict:
     """moe_route without a workspace (the logits use the library's fixed
     device array; T * E <= 1048576; concurrent calls on one device race)."""
     fn = _lib.moe_route_noalloc
-    fn.restype = I32
-    fn.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P, P, P]
     _bits(u, torch.bfloat16)
     _dev(u, "u")
     T, d = u.shape

@@ -129,20 +129,42 @@ int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, v
  *                          rounding), else 0,
  *   counts [E] int32       selections per expert (overwritten).
  * u [T, d] bf16; centroids [E, d]; bias [E].  1 <= K <= min(E, 32),
- * E <= 1024.  Logits are float32 sums with compensation (error about one
- * float32 rounding).  Workspace: at least T * E * 4 bytes (the logits),
- * 16-byte aligned. */
+ * E <= 1024.  The logits that decide the selection and the gates are float32
+ * sums with compensation (error about one float32 rounding): every logit is
+ * first estimated on the tensor cores (bf16 token row against a two-piece
+ * bf16 split of the centroid), and the experts whose estimate lies within the
+ * estimate's error bound of the K-th biased score are recomputed exactly.
+ * Workspace: at least moe_route_workspace_size(T, d, E) bytes, 256-byte
+ * aligned; its first int32 is this call's device status word (0, or
+ * MOE_ERR_TIMEOUT when a bounded device wait gave up; read it with
+ * moe_check_device_status(ws, stream)). */
 int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
               int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
               void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes moe_route needs for T tokens, hidden size d and E experts
+ * (0 for invalid sizes). */
+size_t moe_route_workspace_size(int T, int d, int E);
+
+/* Check hook for moe_route's screening step (no counterpart in the pages):
+ * writes the tensor-core logit estimates l~ [T, E] float32 to logits and the
+ * largest centroid norm (as used in the error bound) to cmax [1] float32,
+ * both device memory.  moe_route treats |l~ - l| <= 2^-11 |u_t| cmax as the
+ * estimate's error bound.  Same workspace rules as moe_route. */
+int moe_route_estimate_logits(const uint16_t* u, const float* centroids, int T, int d, int E,
+                              float* logits, float* cmax, void* ws, size_t ws_bytes,
+                              void* stream);
 
 /* moe_route without a workspace, for callers that cannot allocate device
  * memory when they route (a serving engine whose memory pool owns the whole
  * device, a runtime whose allocator is out of reach of the launching thread,
  * or code that must not allocate between two points it measures or
  * captures).  The pages have no counterpart of this call: it is a service of
- * this library, not a step of the method.  Same arguments, outputs and
- * arithmetic as moe_route, minus ws/ws_bytes; the [T, E] logits live in a
+ * this library, not a step of the method.  Same arguments and outputs as
+ * moe_route, minus ws/ws_bytes; every logit is computed on the CUDA cores
+ * with the same compensated summation (so results agree with moe_route up
+ * to float32 rounding: selections may differ only on flagged near-ties, gates
+ * by a few ulps).  The [T, E] logits live in a
  * fixed 4 MB array in the library's device memory, so T * E must be at most
  * 1048576 (MOE_ERR_WORKSPACE otherwise).  The first call on each device looks
  * up that array's device address (cudaGetSymbolAddress); make that first call

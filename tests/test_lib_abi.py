@@ -38,6 +38,32 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib.lib(), n), n
 
 
+def declared_params():
+    """name -> number of parameters, from the declarations in include/*.h."""
+    out = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            for m in re.finditer(r"\b(moe_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+                params = m.group(2).strip()
+                out[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return out
+
+
+def test_every_entry_point_has_its_ctypes_signature(lib):
+    # ctypes passes Python ints as C int unless argtypes say otherwise, which
+    # cuts device pointers to 32 bits: every declared call must be typed, with
+    # as many argument types as the declaration has parameters
+    params = declared_params()
+    assert set(params) == set(declared())
+    for name, n in params.items():
+        fn = getattr(lib.lib(), name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        assert fn.restype is not None, name
+
+
 def test_status_strings(lib):
     L = lib.lib()
     assert L.moe_status_string(0) == b"ok"
