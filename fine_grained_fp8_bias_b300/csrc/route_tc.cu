@@ -50,7 +50,7 @@ constexpr int RT_THREADS = 128;
 constexpr uint32_t RT_TMEM_COLS = 128;
 constexpr int CAND_CAP = 32;
 constexpr float GAMMA = 0x1p-11f;
-constexpr int SEL_WARPS = 4;                        // tokens per select_refine block
+constexpr int SEL_WARPS = 4;                        // warps per token in select_refine
 
 struct RtCtl {
     uint64_t full[RT_STAGES];
@@ -103,38 +103,42 @@ __device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
 }
 
 // ------------------------------------------------------------ 1. split
-// One warp per expert row: hi/mid pieces and |c_e|; the largest norm (times
+// One block per expert row: hi/mid pieces and |c_e|; the largest norm (times
 // 1 + 2^-20 for its own rounding) goes to *cmax_bits with an integer max,
 // which orders non-negative floats correctly.
-__global__ void __launch_bounds__(256) split_centroids_kernel(const float* __restrict__ c, int E,
-                                                              int d, uint16_t* __restrict__ hi,
-                                                              uint16_t* __restrict__ mid,
-                                                              unsigned int* __restrict__ cmax_bits) {
-    const int lane = threadIdx.x & 31;
-    const int nw = gridDim.x * (blockDim.x >> 5);
-    for (int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); e < E; e += nw) {
-        float ss = 0.0f;
-        for (int j = lane * 4; j < d; j += 128) {
-            const size_t at = (size_t)e * d + j;
-            const float4 v = *reinterpret_cast<const float4*>(c + at);
-            const float x[4] = {v.x, v.y, v.z, v.w};
-            uint16_t h[4], m[4];
+constexpr int SPLIT_THREADS = 256;
+__global__ void __launch_bounds__(SPLIT_THREADS) split_centroids_kernel(
+    const float* __restrict__ c, int E, int d, uint16_t* __restrict__ hi,
+    uint16_t* __restrict__ mid, unsigned int* __restrict__ cmax_bits) {
+    __shared__ float wsum[SPLIT_THREADS / 32];
+    const int e = blockIdx.x;
+    float ss = 0.0f;
+    for (int j = threadIdx.x * 4; j < d; j += SPLIT_THREADS * 4) {
+        const size_t at = (size_t)e * d + j;
+        const float4 v = *reinterpret_cast<const float4*>(c + at);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        uint16_t h[4], m[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat16 bh = __float2bfloat16_rn(x[i]);
-                const __nv_bfloat16 bm = __float2bfloat16_rn(x[i] - __bfloat162float(bh));
-                h[i] = __bfloat16_as_ushort(bh);
-                m[i] = __bfloat16_as_ushort(bm);
-                ss = fmaf(x[i], x[i], ss);
-            }
-            *reinterpret_cast<uint2*>(hi + at) =
-                make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
-            *reinterpret_cast<uint2*>(mid + at) =
-                make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat16 bh = __float2bfloat16_rn(x[i]);
+            const __nv_bfloat16 bm = __float2bfloat16_rn(x[i] - __bfloat162float(bh));
+            h[i] = __bfloat16_as_ushort(bh);
+            m[i] = __bfloat16_as_ushort(bm);
+            ss = fmaf(x[i], x[i], ss);
         }
+        *reinterpret_cast<uint2*>(hi + at) =
+            make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+        *reinterpret_cast<uint2*>(mid + at) =
+            make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+    }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) atomicMax(cmax_bits, __float_as_uint(sqrtf(ss) * (1.0f + 0x1p-20f)));
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = 0; w < SPLIT_THREADS / 32; ++w) t += wsum[w];
+        atomicMax(cmax_bits, __float_as_uint(sqrtf(t) * (1.0f + 0x1p-20f)));
     }
 }
 
@@ -255,30 +259,33 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 // l = u_t . c_e with compensated summation.  Lane L takes elements
 // 128 i + 4 L .. + 3; each 32-product FMA chain starts from zero and is added
 // into (acc, cmp) with TwoSum; the lanes' pairs are then combined with TwoSum
-// too (the xor butterfly leaves the same value in every lane).
+// too (the xor butterfly leaves the same value in every lane).  The centroid
+// loads of the next 8 blocks are issued before the current ones are used.
 __device__ __forceinline__ float exact_dot(const uint16_t* ut, const float* __restrict__ crow,
                                            int d, int lane) {
-    float acc = 0.0f, cmp = 0.0f;
     const int nblk = d / 128;
+    float acc = 0.0f, cmp = 0.0f;
+    float4 nxt[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (q < nblk) nxt[q] = __ldg(reinterpret_cast<const float4*>(crow + q * 128 + lane * 4));
     for (int i = 0; i < nblk; i += 8) {
         float4 cv[8];
-        uint2 uv[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (i + q < nblk) {
-                const int j = (i + q) * 128 + lane * 4;
-                cv[q] = __ldg(reinterpret_cast<const float4*>(crow + j));
-                uv[q] = *reinterpret_cast<const uint2*>(ut + j);
-            }
-        }
+        for (int q = 0; q < 8; ++q) cv[q] = nxt[q];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (i + 8 + q < nblk)
+                nxt[q] = __ldg(reinterpret_cast<const float4*>(crow + (i + 8 + q) * 128 + lane * 4));
         float p = 0.0f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (i + q < nblk) {
-                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].x & 0xFFFFu)), cv[q].x, p);
-                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].x >> 16)), cv[q].y, p);
-                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].y & 0xFFFFu)), cv[q].z, p);
-                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].y >> 16)), cv[q].w, p);
+                const uint2 uv = *reinterpret_cast<const uint2*>(ut + (i + q) * 128 + lane * 4);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv.x & 0xFFFFu)), cv[q].x, p);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv.x >> 16)), cv[q].y, p);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv.y & 0xFFFFu)), cv[q].z, p);
+                p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv.y >> 16)), cv[q].w, p);
             }
         }
         float err;
@@ -323,20 +330,30 @@ __device__ __forceinline__ float kth_largest(const float (&z)[NV], int E, int K,
     return zk;
 }
 
+// One block of SEL_WARPS warps per token.  The token row goes to shared
+// memory once; warp 0 screens the estimates and lists the candidates (in
+// expert order); the warps share the candidates' exact dot products; warp 0
+// selects.  Dynamic shared memory: u_t [d] bf16, then the candidate list
+// (expert, s, z) of up to 32 * NV entries.
 template <int NV>
 __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
     const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
     const float* __restrict__ part, int split, int T, int d, int E, int K,
     const unsigned int* __restrict__ cmax_bits, int32_t* __restrict__ idx, float* __restrict__ gate,
     uint8_t* __restrict__ tie, int32_t* __restrict__ counts) {
-    extern __shared__ __align__(16) uint16_t u_sm[];
+    extern __shared__ __align__(16) uint8_t sel_sm[];
+    __shared__ float red[SEL_WARPS];
+    __shared__ int n_cand;
+    uint16_t* ut = reinterpret_cast<uint16_t*>(sel_sm);
+    int* ce = reinterpret_cast<int*>(sel_sm + (size_t)d * 2);
+    float* cs = reinterpret_cast<float*>(ce + NV * 32);
+    float* cz = cs + NV * 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t = blockIdx.x * SEL_WARPS + warp;
-    if (t >= T) return;
-    uint16_t* ut = u_sm + (size_t)warp * d;
+    const int t = blockIdx.x;
+
     // token row to shared memory, and |u_t|^2
     float ss = 0.0f;
-    for (int j = lane * 8; j < d; j += 256) {
+    for (int j = threadIdx.x * 8; j < d; j += SEL_WARPS * 32 * 8) {
         const uint4 v = *reinterpret_cast<const uint4*>(u + (size_t)t * d + j);
         *reinterpret_cast<uint4*>(ut + j) = v;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -349,59 +366,81 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    __syncwarp();
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
 
-    // approximate biased scores and the candidate band
-    float za[NV];
+    if (warp == 0) {
+        ss = 0.0f;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        const int e = j * 32 + lane;
-        if (e < E) {
-            float l = 0.0f;
-            for (int s = 0; s < split; ++s) l += part[((size_t)s * T + t) * E + e];
-            za[j] = sigmoid(l) + bias[e];
-        } else {
-            za[j] = -FLT_MAX;
-        }
-    }
-    const float zk_approx = kth_largest(za, E, K, lane);
-    const float eps_l = GAMMA * sqrtf(ss) * __uint_as_float(*cmax_bits);
-    const float eps_z = 0.25f * eps_l + 1e-6f + 0x1p-22f * (fabsf(zk_approx) + 1.0f);
-    const float thr = zk_approx - 2.0f * eps_z - 2e-6f;
-    unsigned cand = 0;
+        for (int w = 0; w < SEL_WARPS; ++w) ss += red[w];
+        // approximate biased scores and the candidate band
+        float za[NV];
 #pragma unroll
-    for (int j = 0; j < NV; ++j)
-        if (j * 32 + lane < E && za[j] >= thr) cand |= 1u << j;
-    int n = __popc(cand);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-    if (n > CAND_CAP) {
-        cand = 0;
-#pragma unroll
-        for (int j = 0; j < NV; ++j)
-            if (j * 32 + lane < E) cand |= 1u << j;
-    }
-
-    // exact scores of the candidates
-    float s[NV], z[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        s[j] = 0.0f;
-        z[j] = -FLT_MAX;
-        unsigned m = __ballot_sync(0xffffffffu, (cand >> j) & 1u);
-        while (m) {
-            const int src = __ffs(m) - 1;
-            m &= m - 1;
-            const int e = j * 32 + src;
-            const float l = exact_dot(ut, c + (size_t)e * d, d, lane);
-            if (lane == src) {
-                s[j] = sigmoid(l);
-                z[j] = s[j] + bias[e];
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if (e < E) {
+                float l = 0.0f;
+                for (int s = 0; s < split; ++s) l += part[((size_t)s * T + t) * E + e];
+                za[j] = sigmoid(l) + bias[e];
+            } else {
+                za[j] = -FLT_MAX;
             }
         }
+        const float zk_approx = kth_largest(za, E, K, lane);
+        const float eps_l = GAMMA * sqrtf(ss) * __uint_as_float(*cmax_bits);
+        const float eps_z = 0.25f * eps_l + 1e-6f + 0x1p-22f * (fabsf(zk_approx) + 1.0f);
+        const float thr = zk_approx - 2.0f * eps_z - 2e-6f;
+        unsigned cand = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            if (j * 32 + lane < E && za[j] >= thr) cand |= 1u << j;
+        int n = __popc(cand);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+        if (n > CAND_CAP) {
+            cand = 0;
+#pragma unroll
+            for (int j = 0; j < NV; ++j)
+                if (j * 32 + lane < E) cand |= 1u << j;
+        }
+        // compact the candidates into ce[] in expert order
+        int base = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const unsigned m = __ballot_sync(0xffffffffu, (cand >> j) & 1u);
+            if ((cand >> j) & 1u) ce[base + __popc(m & ((1u << lane) - 1u))] = j * 32 + lane;
+            base += __popc(m);
+        }
+        if (lane == 0) n_cand = base;
     }
+    __syncthreads();
 
-    // selection over the candidates (the others score -FLT_MAX)
+    // exact scores of the candidates, shared among the warps
+    const int nc = n_cand;
+    for (int k = warp; k < nc; k += SEL_WARPS) {
+        const int e = ce[k];
+        const float l = exact_dot(ut, c + (size_t)e * d, d, lane);
+        if (lane == 0) {
+            const float sv = sigmoid(l);
+            cs[k] = sv;
+            cz[k] = sv + bias[e];
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+
+    // selection over the candidates
+    float s[NV], z[NV];
+    int ex[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int k = j * 32 + lane;
+        if (k < nc) {
+            s[j] = cs[k]; z[j] = cz[k]; ex[j] = ce[k];
+        } else {
+            s[j] = 0.0f; z[j] = -FLT_MAX; ex[j] = 0x7fffffff;
+        }
+    }
     unsigned taken = 0;
     float my_s = 0.0f, ssum = 0.0f, zk = 0.0f, zk1 = -FLT_MAX;
     int my_e = -1;
@@ -412,9 +451,8 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
         float bs = 0.0f;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            const int e = j * 32 + lane;
-            if ((cand >> j & 1u) && !(taken >> j & 1u) && better(z[j], e, bz, be)) {
-                bz = z[j]; be = e; bj = j; bs = s[j];
+            if (j * 32 + lane < nc && !(taken >> j & 1u) && better(z[j], ex[j], bz, be)) {
+                bz = z[j]; be = ex[j]; bj = j; bs = s[j];
             }
         }
         float wz = bz, ws = bs;
@@ -447,14 +485,14 @@ template <int NV>
 int launch_select(const uint16_t* u, const float* c, const float* bias, const float* part,
                   int split, int T, int d, int E, int K, const unsigned int* cmax, int32_t* idx,
                   float* gate, uint8_t* tie, int32_t* counts, cudaStream_t st) {
-    const size_t smem = (size_t)SEL_WARPS * d * sizeof(uint16_t);
+    const size_t smem = (size_t)d * 2 + (size_t)NV * 32 * 12;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_refine_kernel<NV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    select_refine_kernel<NV><<<(T + SEL_WARPS - 1) / SEL_WARPS, SEL_WARPS * 32, smem, st>>>(
-        u, c, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts);
+    select_refine_kernel<NV><<<T, SEL_WARPS * 32, smem, st>>>(u, c, bias, part, split, T, d, E, K,
+                                                             cmax, idx, gate, tie, counts);
     return check_launch();
 }
 
@@ -481,7 +519,7 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
     cudaError_t e = cudaMemsetAsync(cmax, 0, sizeof(unsigned int), st);
     if (e != cudaSuccess) return cuda_fail(e);
     int rc;
-    split_centroids_kernel<<<(E + 7) / 8, 256, 0, st>>>(cent, E, d, hi, mid, cmax);
+    split_centroids_kernel<<<E, SPLIT_THREADS, 0, st>>>(cent, E, d, hi, mid, cmax);
     if ((rc = check_launch())) return rc;
     static bool attr_set = false;
     if (!attr_set) {
