@@ -231,9 +231,16 @@ int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
     return launch_combine(u, Y, topk_gate, inv_row, Y_shared, T, d, K, S, h_out, S_(stream));
 }
 
-int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
-                float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
-                void* stream) {
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// moe_forward's body; reset_status = false keeps the status word of earlier
+// calls (moe_forward_host clears it once for its whole batch sequence).
+int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
+                 float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
+                 cudaStream_t st, bool reset_status) {
     int rc = check_layer(L);
     if (rc) return rc;
     if (T < 0) return MOE_ERR_INVALID_ARG;
@@ -246,7 +253,6 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     const Layout W = layout(T, d, E, K, S, I);
     if (ws_bytes < W.total) return MOE_ERR_WORKSPACE;
     char* base = static_cast<char*>(ws);
-    const cudaStream_t st = S_(stream);
     int32_t* status = reinterpret_cast<int32_t*>(base + W.status);
     void* route_ws = base + W.route;
     int32_t* hist = reinterpret_cast<int32_t*>(base + W.hist);
@@ -262,8 +268,10 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
     uint16_t* Y = reinterpret_cast<uint16_t*>(base + W.Y);
     const int M = T * (K + S);
 
-    cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (reset_status) {
+        const cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     if ((rc = launch_route_tc(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
                               counts, route_ws, status, st)))
         return rc;
@@ -279,6 +287,86 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
                                   nullptr, d, I, Y, nullptr, status, st)))
         return rc;
     return launch_combine(u, Y, topk_gate, inv_row, Y + (size_t)T * K * d, T, d, K, S, h_out, st);
+}
+
+struct EventSet {
+    cudaEvent_t ev[6] = {};
+    ~EventSet() {
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);   // released when their last record completes
+    }
+};
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
+                float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
+                void* stream) {
+    return forward_impl(L, u, T, h_out, topk_idx, topk_gate, counts, tie_flag, ws, ws_bytes,
+                        S_(stream), true);
+}
+
+int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t* const* u_host,
+                     float* const* h_host, float gamma, const moe_batch_buffers_t* buf, void* ws,
+                     size_t ws_bytes, void* compute_stream, void* h2d_stream, void* d2h_stream) {
+    int rc = check_layer(L);
+    if (rc) return rc;
+    if (T < 0 || n_batches < 0) return MOE_ERR_INVALID_ARG;
+    if (n_batches == 0) return MOE_OK;
+    if (!u_host || !h_host || !buf || !ws) return MOE_ERR_INVALID_ARG;
+    for (int k = 0; k < n_batches; ++k)
+        if (T > 0 && (!u_host[k] || !h_host[k])) return MOE_ERR_INVALID_ARG;
+    for (int s = 0; s < 2; ++s) {
+        const moe_batch_buffers_t& b = buf[s];
+        if (!b.counts || (T > 0 && (!b.u || !b.h || !b.topk_idx || !b.topk_gate || !b.tie_flag)))
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned16(b.u) || !aligned16(b.h)) return MOE_ERR_MISALIGNED;
+    }
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < layout(T, L->d, L->E, L->K, L->S, L->I).total) return MOE_ERR_WORKSPACE;
+    const cudaStream_t cs = S_(compute_stream), up = S_(h2d_stream), down = S_(d2h_stream);
+    EventSet E;
+    cudaEvent_t* h2d_done = E.ev;          // [2] batch k's tokens are on the device
+    cudaEvent_t* fwd_done = E.ev + 2;      // [2] batch k's forward (and bias step) finished
+    cudaEvent_t* d2h_done = E.ev + 4;      // [2] batch k's output is in host memory
+    cudaError_t e;
+    for (cudaEvent_t& ev : E.ev)
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e);
+    int32_t* status = static_cast<int32_t*>(ws);
+    if ((e = cudaMemsetAsync(status, 0, 16, cs)) != cudaSuccess) return cuda_fail(e);
+    const size_t u_bytes = sizeof(uint16_t) * (size_t)T * L->d;
+    const size_t h_bytes = sizeof(float) * (size_t)T * L->d;
+    for (int k = 0; k < n_batches; ++k) {
+        const int s = k & 1;
+        const moe_batch_buffers_t& b = buf[s];
+        // upload into slot s once batch k-2's forward has read it
+        if (k >= 2 && (e = cudaStreamWaitEvent(up, fwd_done[s], 0)) != cudaSuccess) return cuda_fail(e);
+        if (T > 0 && (e = cudaMemcpyAsync(b.u, u_host[k], u_bytes, cudaMemcpyHostToDevice, up)) !=
+                         cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaEventRecord(h2d_done[s], up)) != cudaSuccess) return cuda_fail(e);
+        // forward once the tokens are there and slot s's output has been read back
+        if ((e = cudaStreamWaitEvent(cs, h2d_done[s], 0)) != cudaSuccess) return cuda_fail(e);
+        if (k >= 2 && (e = cudaStreamWaitEvent(cs, d2h_done[s], 0)) != cudaSuccess) return cuda_fail(e);
+        if ((rc = forward_impl(L, b.u, T, b.h, b.topk_idx, b.topk_gate, b.counts, b.tie_flag, ws,
+                               ws_bytes, cs, false)))
+            return rc;
+        if (gamma != 0.0f &&
+            (rc = launch_update_bias(b.counts, L->E, T, L->K, gamma, const_cast<float*>(L->bias), cs)))
+            return rc;
+        if ((e = cudaEventRecord(fwd_done[s], cs)) != cudaSuccess) return cuda_fail(e);
+        // download
+        if ((e = cudaStreamWaitEvent(down, fwd_done[s], 0)) != cudaSuccess) return cuda_fail(e);
+        if (T > 0 && (e = cudaMemcpyAsync(h_host[k], b.h, h_bytes, cudaMemcpyDeviceToHost, down)) !=
+                         cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaEventRecord(d2h_done[s], down)) != cudaSuccess) return cuda_fail(e);
+    }
+    return MOE_OK;
 }
 
 int moe_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,

@@ -79,6 +79,32 @@ class MoELayer:
         out = self.outputs(T) if out is None else out
         return lib.moe_forward(self.struct(), u, self.workspace(T), out, stream)
 
+    def forward_host(self, u_host: list, h_host: list, gamma: float = 0.0, streams=None) -> list:
+        """The layer over batches that live in pinned host memory, pipelined
+        (moe_forward_host): batch k+1's upload and batch k-1's download overlap
+        batch k's compute; with gamma != 0 the bias steps after every batch.
+        Returns the two device buffer sets (the last two batches' routing).
+        Asynchronous on the three streams (created here unless given)."""
+        T = u_host[0].shape[0] if u_host else 0
+        if streams is None:
+            streams = getattr(self, "_host_streams", None)
+            if streams is None:
+                streams = self._host_streams = (torch.cuda.Stream(self.device),
+                                                torch.cuda.Stream(self.device),
+                                                torch.cuda.Stream(self.device))
+        bufs = getattr(self, "_host_bufs", None)
+        if bufs is None or bufs[0]["u"].shape[0] != T:
+            bufs = self._host_bufs = [dict(self.outputs(T),
+                                           u=torch.empty((T, self.d), dtype=torch.bfloat16,
+                                                         device=self.device)) for _ in range(2)]
+        # the streams start after everything already queued on the current one
+        cur = torch.cuda.current_stream(self.device)
+        for s in streams:
+            s.wait_stream(cur)
+        lib.moe_forward_host(self.struct(), T, u_host, h_host, gamma, bufs, self.workspace(T),
+                             *streams)
+        return bufs
+
     def update_bias(self, counts: torch.Tensor, T: int, gamma: float, stream=None):
         lib.moe_update_bias(counts, self.bias, T, self.K, gamma, stream)
 

@@ -40,6 +40,11 @@ class moe_layer_t(ctypes.Structure):
                 ("s_gate", P), ("s_up", P), ("s_down", P)]
 
 
+class moe_batch_buffers_t(ctypes.Structure):
+    _fields_ = [("u", P), ("h", P), ("topk_idx", P), ("topk_gate", P), ("tie_flag", P),
+                ("counts", P)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libmoefp8.so is not built ({LIB_PATH}); run __graft_entry__.build()")
@@ -69,6 +74,8 @@ def _load() -> ctypes.CDLL:
         "moe_combine": [P, P, P, P, P, I32, I32, I32, I32, P, P],
         "moe_forward": [ctypes.POINTER(moe_layer_t), P, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_update_bias": [P, I32, I32, I32, ctypes.c_float, P, P],
+        "moe_forward_host": [ctypes.POINTER(moe_layer_t), I32, I32, P, P, ctypes.c_float,
+                             ctypes.POINTER(moe_batch_buffers_t), P, ctypes.c_size_t, P, P, P],
         "moe_check_device_status": [P, P],
     }
     for name, args in sigs.items():
@@ -317,3 +324,32 @@ def moe_forward(layer: moe_layer_t, u: torch.Tensor, ws: torch.Tensor, out: dict
                             _ptr(out["gate"]), _ptr(out["counts"]), _ptr(out["tie"]), _ptr(ws),
                             ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
     return out
+
+
+def moe_forward_host(L: moe_layer_t, T: int, u_host: list, h_host: list, gamma: float,
+                     bufs: list, ws: torch.Tensor, compute_stream=None, h2d_stream=None,
+                     d2h_stream=None) -> None:
+    """moe_forward_host: the layer over the batches u_host[k] (pinned [T, d]
+    bf16 host tensors), outputs to h_host[k] (pinned [T, d] float32), with
+    uploads, compute and downloads on three streams.  bufs: two dicts of
+    device tensors with keys u, h, idx, gate, tie, counts.  Asynchronous:
+    synchronise d2h_stream before reading h_host."""
+    n = len(u_host)
+    if len(h_host) != n or len(bufs) != 2:
+        raise ValueError("need one output per batch and two buffer sets")
+    for t in u_host:
+        _bits(t, torch.bfloat16)
+        if t.is_cuda:
+            raise ValueError("u_host must be host tensors")
+    for t in h_host:
+        if t.is_cuda or t.dtype != torch.float32:
+            raise ValueError("h_host must be float32 host tensors")
+    u_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in u_host])
+    h_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in h_host])
+    b_arr = (moe_batch_buffers_t * 2)(*[moe_batch_buffers_t(_ptr(b["u"]), _ptr(b["h"]), _ptr(b["idx"]),
+                                                            _ptr(b["gate"]), _ptr(b["tie"]),
+                                                            _ptr(b["counts"])) for b in bufs])
+    _check(_lib.moe_forward_host(ctypes.byref(L), T, n, ctypes.cast(u_arr, P),
+                                 ctypes.cast(h_arr, P), gamma, b_arr, _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(compute_stream),
+                                 _stream(h2d_stream), _stream(d2h_stream)), "moe_forward_host")

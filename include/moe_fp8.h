@@ -238,6 +238,37 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
                 float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* Device buffers of one batch in flight for moe_forward_host (caller-owned,
+ * device memory): u [T, d] bf16, h [T, d] float32 (16-byte aligned),
+ * topk_idx [T, K] int32, topk_gate [T, K] float32, tie_flag [T] uint8,
+ * counts [E] int32. */
+typedef struct moe_batch_buffers_t {
+    uint16_t* u;
+    float* h;
+    int32_t* topk_idx;
+    float* topk_gate;
+    uint8_t* tie_flag;
+    int32_t* counts;
+} moe_batch_buffers_t;
+
+/* The layer over a sequence of n_batches batches of T tokens held in host
+ * memory (page-locked, so the copies run asynchronously): for batch k,
+ * u_host[k] [T, d] bf16 goes to buf[k % 2].u on h2d_stream, moe_forward runs
+ * on compute_stream, then -- when gamma != 0 -- moe_update_bias with that
+ * batch's counts (the next batch is routed with the updated bias), and
+ * buf[k % 2].h goes back to h_host[k] [T, d] float32 on d2h_stream.  Events
+ * (created and released by the call) order the three streams so that the
+ * upload of batch k+1 and the download of batch k-1 overlap the compute of
+ * batch k; the batches share ws (moe_workspace_size(L, T) bytes, 256-byte
+ * aligned), whose status word is cleared once and then collects every
+ * batch's device errors.  Nothing synchronises the host: synchronise
+ * d2h_stream before reading h_host.  With the same stream passed three times
+ * the batches run one after another.  The pages describe no host interface;
+ * this is a service of the library for inputs that arrive from the host. */
+int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t* const* u_host,
+                     float* const* h_host, float gamma, const moe_batch_buffers_t* buf, void* ws,
+                     size_t ws_bytes, void* compute_stream, void* h2d_stream, void* d2h_stream);
+
 /* Auxiliary-loss-free bias update at the end of a step ([TH] Method §2:
  * b_i -= gamma when expert i is overloaded, += gamma when underloaded;
  * gamma = 0.001 there).  With n = T*K selections, expert e is overloaded when

@@ -104,3 +104,37 @@ def test_forward_is_deterministic():
     b = L.forward(u)
     torch.cuda.synchronize()
     assert torch.equal(h1, b["h"])
+
+
+@pytest.mark.parametrize("name,n", [("tiny", 5), ("ragged", 4)])
+def test_forward_host_pipeline_matches_sequential_calls(name, n):
+    # moe_forward_host overlaps uploads, compute and downloads on three streams
+    # with two device buffer sets; it must give exactly what moe_forward +
+    # moe_update_bias give batch after batch (the bias moves between batches)
+    from fine_grained_fp8_bias_b300.layer import MoELayer
+    cfg = wl.TINY if name == "tiny" else wl.LayerConfig("ragged", T=301, d=640, E=24, K=3, S=2,
+                                                        I=384, seed=23)
+    gamma = 0.01
+    seq = MoELayer.from_config(cfg, "cuda")
+    pipe = MoELayer.from_config(cfg, "cuda")
+    batches = [wl.tokens(cfg, "cpu", step=k) for k in range(n)]
+    ref_h, ref_idx = [], []
+    for u in batches:
+        out = seq.forward(u.cuda())
+        seq.update_bias(out["counts"], cfg.T, gamma)
+        ref_h.append(out["h"].cpu())
+        ref_idx.append(out["idx"].cpu())
+    torch.cuda.synchronize()
+    u_host = [wl.pinned_like(u) for u in batches]
+    h_host = [torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32, pin_memory=True)
+              for _ in range(n)]
+    bufs = pipe.forward_host(u_host, h_host, gamma)
+    torch.cuda.synchronize()
+    assert pipe.status() == 0
+    for k in range(n):
+        assert torch.equal(h_host[k], ref_h[k]), k
+    # the last two batches' routing stays in the two buffer sets
+    for k in (n - 2, n - 1):
+        assert torch.equal(bufs[k % 2]["idx"].cpu(), ref_idx[k])
+    assert torch.equal(pipe.bias, seq.bias)
+    assert not torch.equal(pipe.bias, wl.bias(cfg).cuda())      # the bias did move
