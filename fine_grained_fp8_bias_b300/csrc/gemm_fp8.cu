@@ -59,6 +59,8 @@ constexpr int NUM_THREADS = 128 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;             // 2 buffers x 256 fp32 columns
 constexpr int SCALE_SLOTS = 8;                  // depth of the scale ring
 constexpr int SCALE_LAG = 3;                    // copy groups in flight before a slab is published
+constexpr int TILE_SLOTS = 4;                   // depth of the tile-index ring
+constexpr int TILE_READERS = 2 + NUM_EPI_WARPS; // MMA thread, scale loader, epilogue warps
 // Register split: the kernel is compiled for 384 threads x 168 registers
 // (64512); warpgroup 0 drops to 40 and the two epilogue warpgroups rise to
 // 232: 128 * 40 + 256 * 232 = 64512.  Per SM sub-partition (warps w, w+4,
@@ -83,6 +85,9 @@ struct alignas(16) Ctl {
     uint64_t epi_done;                          // every epilogue warp finished with TMEM
     uint64_t sfull[SCALE_SLOTS];
     uint64_t sempty[SCALE_SLOTS];
+    uint64_t tile_full[TILE_SLOTS];
+    uint64_t tile_empty[TILE_SLOTS];
+    int tile_ring[TILE_SLOTS];                  // tile indices in processing order; -1 ends
     uint32_t tmem_base;
     int abort;
     int total_tiles;
@@ -108,6 +113,7 @@ struct Params {
     void* out;
     float* out_scales;
     int32_t* status;
+    int* counter;                               // next unclaimed tile (nullable: static order)
 };
 
 // ----------------------------------------------------------- tile lookup
@@ -144,6 +150,26 @@ __device__ __forceinline__ uint32_t quant4_rcp(float a, float b, float c, float 
     const uint32_t lo = e4m3x2(div_rcp(a, scale, r), div_rcp(b, scale, r));
     const uint32_t hi = e4m3x2(div_rcp(c, scale, r), div_rcp(d, scale, r));
     return lo | (hi << 16);
+}
+
+// The next tile index from the ring (-1: no more tiles); false when the wait
+// gave up.  Single-thread form (MMA issuer) and warp form.
+__device__ __forceinline__ bool take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status) {
+    const int slot = tpos % TILE_SLOTS;
+    if (!mbar_wait(&ctl->tile_full[slot], (tpos / TILE_SLOTS) & 1, &ctl->abort, status)) return false;
+    tile = ctl->tile_ring[slot];
+    mbar_arrive(&ctl->tile_empty[slot]);
+    ++tpos;
+    return true;
+}
+__device__ __forceinline__ bool warp_take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status) {
+    const int slot = tpos % TILE_SLOTS;
+    if (!warp_wait(&ctl->tile_full[slot], (tpos / TILE_SLOTS) & 1, &ctl->abort, status)) return false;
+    tile = ctl->tile_ring[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->tile_empty[slot]);
+    ++tpos;
+    return true;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -201,6 +227,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_init(&ctl->sfull[s], 32);   // one arrival per loader lane
                 mbar_init(&ctl->sempty[s], NUM_EPI_WARPS);
             }
+            for (int s = 0; s < TILE_SLOTS; ++s) {
+                mbar_init(&ctl->tile_full[s], 1);
+                mbar_init(&ctl->tile_empty[s], TILE_READERS);
+            }
             mbar_init(&ctl->xbar, NUM_EPI_WARPS);
             mbar_init(&ctl->epi_done, NUM_EPI_WARPS);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -228,9 +258,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t it = 0, tpos = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            int tile = -1;
+            while (ok) {
+                // claim the next tile (adjacent claims share a weight panel, so
+                // CTAs that claim them together stream it from HBM once) and
+                // publish it to the other roles
+                int next = p.counter ? atomicAdd(p.counter, 1)
+                                     : (tile < 0 ? (int)blockIdx.x : tile + (int)gridDim.x);
+                if (next >= total_tiles) next = -1;
+                const int slot = tpos % TILE_SLOTS;
+                if (!mbar_wait(&ctl->tile_empty[slot], ((tpos / TILE_SLOTS) & 1) ^ 1, &ctl->abort,
+                               p.status)) {
+                    ok = false;
+                    break;
+                }
+                ctl->tile_ring[slot] = next;
+                mbar_arrive(&ctl->tile_full[slot]);
+                ++tpos;
+                if (next < 0) break;
+                tile = next;
                 const Tile tl = find_tile(ctl, G, tile);
                 const int a_row = ctl->go[tl.g] + tl.mt * BM;
                 int b0_row, b1_row;
@@ -267,9 +315,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ================= MMA issuer =================
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3(BM, BN);
-            uint32_t it = 0;
+            uint32_t it = 0, tpos = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            int tile;
+            while (ok) {
+                if (!take_tile(ctl, tpos, tile, p.status)) break;
+                if (tile < 0) break;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -304,9 +355,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Slot j of the ring holds slab j's 128 activation scales (row order of
         // the tile, 0 for rows outside the group) and the weight scale of each
         // 128-column half of the output tile.
-        uint32_t it = 0;
+        uint32_t it = 0, tpos = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        int tile;
+        while (ok) {
+            if (!warp_take_tile(ctl, tpos, tile, p.status)) { ok = false; break; }
+            if (tile < 0) break;
             const Tile tl = find_tile(ctl, G, tile);
             const int g0 = ctl->go[tl.g];
             const int m_g = max(0, ctl->go[tl.g + 1] - g0);
@@ -367,10 +421,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;             // TMEM lane quarter
         const int row = quarter * 32 + lane;      // row within the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t it = 0;
+        uint32_t it = 0, tpos = 0;
         int tcount = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
+        int tile;
+        for (; ok; ++tcount) {
+            if (!warp_take_tile(ctl, tpos, tile, p.status)) { ok = false; break; }
+            if (tile < 0) break;
             const Tile tl = find_tile(ctl, G, tile);
             const int g0 = ctl->go[tl.g];
             const int m_g = max(0, ctl->go[tl.g + 1] - g0);
@@ -574,7 +631,14 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
     } else {
         mB1 = mB0;
     }
-    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status};
+    // status[1] is this call's tile counter (dynamic schedule); without a
+    // status buffer the tiles are taken in a fixed order
+    int* counter = status ? status + 1 : nullptr;
+    if (counter) {
+        const cudaError_t ce = cudaMemsetAsync(counter, 0, sizeof(int), st);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+    }
+    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter};
     const int NT = mode == MOE_GEMM_GATE_UP_SILU_QUANT ? N / 128 : (N + BN - 1) / BN;
     const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NT;
     const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);

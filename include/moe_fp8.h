@@ -209,9 +209,12 @@ int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* of
  *   mode DOWN: W0 = W_down, N = d; out = y [M_total, N] bf16 (round to
  *     nearest even); out_scales unused.
  * Rows outside every group are left untouched.  Kdim and N multiples of 128;
- * G <= 1088; all pointers 16-byte aligned.  status (device int32, nullable)
- * receives MOE_ERR_TIMEOUT if a pipeline wait ran out (the kernel then stops
- * early and its output is incomplete). */
+ * G <= 1088; all pointers 16-byte aligned.  status (device int32 [2],
+ * nullable): status[0] receives MOE_ERR_TIMEOUT if a pipeline wait ran out
+ * (the kernel then stops early and its output is incomplete); status[1] is
+ * the call's tile counter (cleared by the call; the CTAs claim output tiles
+ * from it in order, so tiles that share a weight panel run together).
+ * Without a status buffer the tiles are taken in a fixed order. */
 int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_total,
                          const int32_t* group_offsets, int G, const uint8_t* W0,
                          const uint8_t* W1, const float* sw0, const float* sw1, int N, int Kdim,
