@@ -213,9 +213,9 @@ def gemm_flops(cfg, T) -> dict:
     return {"gemm_gate_up": 2.0 * M * 2 * cfg.I * cfg.d, "gemm_down": 2.0 * M * cfg.d * cfg.I}
 
 
-def kernel_traffic(stage: str):
+def kernel_traffic(stage: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+    current kernel source and the same workload (else None)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
@@ -226,7 +226,7 @@ def kernel_traffic(stage: str):
         return None
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     e = d.get("kernels", {}).get(stage)
-    if e is None or d.get("source_sha256_16") != h:
+    if e is None or d.get("source_sha256_16") != h or d.get("workload_name") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -298,12 +298,28 @@ def run_ours(args, world, rank, local):
             kernels[s]["TFLOPs"] = round(flops[s] / (ms * 1e-3) / 1e12, 1)
     dom = max(STAGES, key=lambda s: per_stage[s])
     dom_ms = per_stage[dom] / args.steps
-    achieved = abytes[dom] / (dom_ms * 1e-3) / 1e9
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": kernel_traffic(dom), "algorithmic_bytes": abytes[dom],
-                "peak_source": f"{pk['source']} HBM copy bandwidth"}
     fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    # The dominant kernel runs inside a long loop of steps: its tensor peak is the
+    # sustained bf16 figure times the nominal FP8:BF16 ratio.  Above the ridge
+    # point (peak FLOP/s over copy bandwidth) it is bound by the tensor pipe.
+    fp8_sustained = (pk.get("bf16_tflops_sustained") or pk["bf16_tflops"]) * FP8_OVER_BF16
+    intensity = flops.get(dom, 0.0) / abytes[dom]
+    ridge = fp8_sustained * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if intensity > ridge:
+        achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / fp8_sustained, 4),
+                    "traffic": kernel_traffic(dom, cfg.name), "algorithmic_flops": flops[dom],
+                    "algorithmic_bytes": abytes[dom], "flop_per_byte": round(intensity, 1),
+                    "peak_source": f"{pk['source']} cuBLAS bf16 sustained x nominal FP8:BF16 ratio 2"}
+    else:
+        achieved = abytes[dom] / (dom_ms * 1e-3) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                    "traffic": kernel_traffic(dom, cfg.name), "algorithmic_bytes": abytes[dom],
+                    "flop_per_byte": round(intensity, 1),
+                    "peak_source": f"{pk['source']} HBM copy bandwidth"}
     fp8 = {s: {"TFLOPs": kernels[s]["TFLOPs"], "frac_of_fp8_peak": round(
         kernels[s]["TFLOPs"] / fp8_peak, 4)} for s in flops}
     fp8["peak_TFLOPs"] = fp8_peak
@@ -311,6 +327,7 @@ def run_ours(args, world, rank, local):
 
     e2e = run_e2e(layer, cfg, dev, max(3, min(args.steps, 50)), world)
     decode = run_decode(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
+    balance = run_balance(layer, cfg, dev) if args.workload == "v3_long" else None
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -324,6 +341,8 @@ def run_ours(args, world, rank, local):
     }
     if decode:
         line["decode"] = decode
+    if balance:
+        line["balance"] = balance
     return line
 
 
@@ -374,6 +393,33 @@ def run_decode(layer, cfg, dev, pk, T=64, steps=50):
     return {"T": T, "us_per_forward": round(us, 1), "experts_touched": touched,
             "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
             "frac_of_hbm": round(wbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4)}
+
+
+def run_balance(layer, cfg, dev, steps=100):
+    """Long-prefill leg: every step routes a fresh batch (generated on the device
+    from the same stream of seeds), runs the layer and the bias update.  Reports
+    the max over experts of c_e / (T K / E) per step and the layer's tokens/s
+    over these steps (CUDA events around forward + bias update only)."""
+    out = layer.outputs(cfg.T)
+    ratios, ms = [], 0.0
+    mean_load = cfg.T * cfg.K / cfg.E
+    for step in range(steps):
+        u = wl.tokens(cfg, dev, step)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        layer.forward(u, out)
+        layer.update_bias(out["counts"], cfg.T, cfg.gamma)
+        e.record()
+        torch.cuda.synchronize()
+        ms += s.elapsed_time(e)
+        ratios.append(float(out["counts"].max().item()) / mean_load)
+    if layer.status() != 0:
+        raise RuntimeError("device status flagged in the balance leg")
+    return {"steps": steps, "tokens_per_s": round(cfg.T * steps / (ms / 1e3), 1),
+            "max_load_over_mean": {"first": round(ratios[0], 3), "last": round(ratios[-1], 3),
+                                   "min": round(min(ratios), 3), "max": round(max(ratios), 3),
+                                   "mean_last_10": round(statistics.mean(ratios[-10:]), 3)},
+            "inputs": "fresh batch per step (4-component mixture), bias updated every step"}
 
 
 # ------------------------------------------------------ CPU oracle arm
