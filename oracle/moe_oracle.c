@@ -48,6 +48,13 @@
  *   R10 bias update: with n = T*K selections, expert e is overloaded when
  *       c_e * E > n and underloaded when c_e * E < n (integer compare);
  *       b_e -= gamma or += gamma in float32; equal load leaves b_e unchanged.
+ *   R14 group-limited routing (the pages: a token goes to at most M = 4
+ *       nodes, no scoring rule given): experts form n_groups contiguous
+ *       groups; group score = float32 sum, largest first, of the group's
+ *       group_topk largest z; keep the topk_groups best groups (equal: lower
+ *       group index); then R4 among the kept groups' experts.  Also flagged
+ *       as a near tie: the last kept and the next group score differ by
+ *       less than 1e-6.
  */
 #include <math.h>
 #include <stdint.h>
@@ -302,6 +309,103 @@ void orc_route(const uint16_t* u, const float* cent, const float* bias,
         tie[t] = (K < E && (zk - zk1) < 1e-6f) ? 1 : 0;
     }
     free(s); free(z); free(taken);
+}
+
+/* ------------------------------------------------------------------ */
+/* Group-limited routing (R14).  The pages: each token is sent to at    */
+/* most M = 4 nodes ("官方揭秘DeepSeek-V3模型训练全流程" §2.2 bullet on  */
+/* node-limited routing; "DeepSeek V3技術報告", table of innovations).    */
+/* Reading: experts form n_groups contiguous groups of E / n_groups      */
+/* (one per node); a group's score is the float32 sum, largest first, of */
+/* its group_topk largest biased scores z = s + b; the topk_groups groups */
+/* with the largest scores are kept (equal scores: lower group index);   */
+/* top-K by z among the kept groups' experts as in orc_route; gates as   */
+/* in orc_route.  tie: the K-th and (K+1)-th kept z differ by < 1e-6, or */
+/* the topk_groups-th and the next group score differ by < 1e-6.         */
+/* ------------------------------------------------------------------ */
+void orc_route_grouped(const uint16_t* u, const float* cent, const float* bias,
+                       int T, int d, int E, int K, int n_groups, int topk_groups,
+                       int group_topk, int32_t* idx, float* gate, uint8_t* tie,
+                       int32_t* counts, float* scores) {
+    const int gsize = E / n_groups;
+    float* s = (float*)malloc(sizeof(float) * (size_t)E);
+    float* z = (float*)malloc(sizeof(float) * (size_t)E);
+    float* gscore = (float*)malloc(sizeof(float) * (size_t)n_groups);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    unsigned char* kept = (unsigned char*)malloc((size_t)n_groups);
+    if (counts) memset(counts, 0, sizeof(int32_t) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        for (int i = 0; i < E; ++i) {
+            double l = 0.0;
+            for (int j = 0; j < d; ++j)
+                l += (double)bf16_to_f32(u[(int64_t)t * d + j]) * (double)cent[(int64_t)i * d + j];
+            float lf = (float)l;
+            s[i] = (float)(1.0 / (1.0 + exp(-(double)lf)));
+            z[i] = s[i] + bias[i];
+            if (scores) scores[(int64_t)t * E + i] = s[i];
+        }
+        /* group scores: group_topk passes of "largest z" inside each group */
+        for (int g = 0; g < n_groups; ++g) {
+            float acc = 0.0f;
+            for (int i = 0; i < E; ++i) taken[i] = 0;
+            for (int k = 0; k < group_topk; ++k) {
+                int best = -1;
+                for (int i = g * gsize; i < (g + 1) * gsize; ++i) {
+                    if (taken[i]) continue;
+                    if (best < 0 || z[i] > z[best]) best = i;
+                }
+                taken[best] = 1;
+                acc += z[best];
+            }
+            gscore[g] = acc;
+            kept[g] = 0;
+        }
+        /* kept groups: topk_groups (+1) passes over the group scores */
+        float gm = 0.0f, gm1 = 0.0f;
+        for (int k = 0; k < topk_groups + 1 && k < n_groups; ++k) {
+            int best = -1;
+            for (int g = 0; g < n_groups; ++g) {
+                if (kept[g] == 1) continue;
+                if (best < 0 || gscore[g] > gscore[best]) best = g;
+            }
+            if (k < topk_groups) {
+                kept[best] = 1;
+                if (k == topk_groups - 1) gm = gscore[best];
+            } else {
+                gm1 = gscore[best];
+            }
+        }
+        /* experts of the other groups are out of the selection */
+        int allowed = 0;
+        for (int i = 0; i < E; ++i) {
+            taken[i] = kept[i / gsize] ? 0 : 1;
+            allowed += !taken[i];
+        }
+        float zk = 0.0f, zk1 = 0.0f;
+        double ssum = 0.0;
+        for (int k = 0; k < K + 1 && k < allowed; ++k) {
+            int best = -1;
+            for (int i = 0; i < E; ++i) {
+                if (taken[i]) continue;
+                if (best < 0 || z[i] > z[best]) best = i;
+            }
+            taken[best] = 1;
+            if (k < K) {
+                idx[(int64_t)t * K + k] = best;
+                ssum += (double)s[best];
+                if (k == K - 1) zk = z[best];
+                if (counts) counts[best] += 1;
+            } else {
+                zk1 = z[best];
+            }
+        }
+        for (int k = 0; k < K; ++k)
+            gate[(int64_t)t * K + k] = (float)((double)s[idx[(int64_t)t * K + k]] / ssum);
+        const int ktie = K < allowed && (zk - zk1) < 1e-6f;
+        const int gtie = topk_groups < n_groups && (gm - gm1) < 1e-6f;
+        tie[t] = (ktie || gtie) ? 1 : 0;
+    }
+    free(s); free(z); free(gscore); free(taken); free(kept);
 }
 
 /* ------------------------------------------------------------------ */

@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
         _lib.orc_expert_ffn.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P]
         _lib.orc_gate_up.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P]
         _lib.orc_route.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P]
+        _lib.orc_route_grouped.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P, P, P]
         _lib.orc_dispatch.restype = i32
         _lib.orc_dispatch.argtypes = [P, i32, i32, i32, P, P, P, P]
         _lib.orc_layer_forward.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P,
@@ -217,6 +218,27 @@ def layer_forward(u_bits, idx, gate, W: Weights, d: int, E: int, K: int, S: int,
                             ptrs(W.gate, 0), ptrs(W.gate, 1), ptrs(W.up, 0), ptrs(W.up, 1),
                             ptrs(W.down, 0), ptrs(W.down, 1), _p(tok), len(tok), _p(out))
     return out
+
+
+def route_grouped(u_bits, cent, bias, K: int, n_groups: int, topk_groups: int,
+                  group_topk: int) -> dict:
+    """Group-limited routing (reading R14): keep the topk_groups groups of
+    E / n_groups experts with the largest sums of their group_topk best biased
+    scores, then top-K among the kept groups' experts."""
+    u_bits, cent, bias = _c(u_bits, np.uint16), _c(cent, np.float32), _c(bias, np.float32)
+    T, d = u_bits.shape
+    E = cent.shape[0]
+    if E % n_groups or not (1 <= topk_groups <= n_groups) or not (1 <= group_topk <= E // n_groups) \
+            or K > topk_groups * (E // n_groups):
+        raise ValueError("bad group configuration")
+    idx = np.empty((T, K), np.int32)
+    gate = np.empty((T, K), np.float32)
+    tie = np.empty((T,), np.uint8)
+    counts = np.empty((E,), np.int32)
+    scores = np.empty((T, E), np.float32)
+    lib().orc_route_grouped(_p(u_bits), _p(cent), _p(bias), T, d, E, K, n_groups, topk_groups,
+                            group_topk, _p(idx), _p(gate), _p(tie), _p(counts), _p(scores))
+    return {"idx": idx, "gate": gate, "tie": tie, "counts": counts, "scores": scores}
 
 
 def update_bias(counts, bias, T: int, K: int, gamma: float) -> np.ndarray:
