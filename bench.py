@@ -162,7 +162,11 @@ class Step:
     def stage(self, name):
         lib, L = self.lib, self.L
         if name == "route":
-            lib.moe_route(self.u, L.centroids, L.bias, L.K, ws=self.route_ws, out=self.rout)
+            if L.n_groups:
+                lib.moe_route_grouped(self.u, L.centroids, L.bias, L.K, L.n_groups, L.topk_groups,
+                                      L.group_topk, ws=self.route_ws, out=self.rout)
+            else:
+                lib.moe_route(self.u, L.centroids, L.bias, L.K, ws=self.route_ws, out=self.rout)
         elif name == "permute":
             lib.moe_permute(self.rout["idx"], L.E, L.S, ws=self.perm_ws, status=self.status,
                             out=self.pout)

@@ -45,6 +45,17 @@ Layout layout(int T, int d, int E, int K, int S, int I) {
     return L;
 }
 
+// Group-limited routing parameters (n_groups = 0 means plain top-K when allowed).
+int check_groups(int E, int K, int n_groups, int topk_groups, int group_topk, bool zero_ok) {
+    if (n_groups == 0 && zero_ok) return MOE_OK;
+    if (n_groups < 1 || n_groups > 32 || E % n_groups) return MOE_ERR_INVALID_ARG;
+    const int gs = E / n_groups;
+    if (topk_groups < 1 || topk_groups > n_groups || group_topk < 1 || group_topk > gs)
+        return MOE_ERR_INVALID_ARG;
+    if (K > topk_groups * gs) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 int check_layer(const moe_layer_t* L) {
     if (!L) return MOE_ERR_INVALID_ARG;
     if (L->d <= 0 || L->E <= 0 || L->K <= 0 || L->S < 0 || L->I <= 0) return MOE_ERR_INVALID_ARG;
@@ -57,7 +68,7 @@ int check_layer(const moe_layer_t* L) {
     if (!aligned16(L->centroids) || !aligned16(L->w_gate) || !aligned16(L->w_up) ||
         !aligned16(L->w_down))
         return MOE_ERR_MISALIGNED;
-    return MOE_OK;
+    return check_groups(L->E, L->K, L->n_groups, L->topk_groups, L->group_topk, true);
 }
 
 inline cudaStream_t S_(void* s) { return static_cast<cudaStream_t>(s); }
@@ -158,6 +169,29 @@ int moe_route_estimate_logits(const uint16_t* u, const float* centroids, int T, 
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), S_(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return launch_route_estimate(u, centroids, T, d, E, logits, cmax, ws, status, S_(stream));
+}
+
+int moe_route_grouped(const uint16_t* u, const float* centroids, const float* bias, int T, int d,
+                      int E, int K, int n_groups, int topk_groups, int group_topk,
+                      int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
+                      void* ws, size_t ws_bytes, void* stream) {
+    if (T < 0 || d <= 0 || E <= 0 || K <= 0 || K > E || K > kMaxTopK || E > kMaxExperts)
+        return MOE_ERR_INVALID_ARG;
+    if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    int rc = check_groups(E, K, n_groups, topk_groups, group_topk, false);
+    if (rc) return rc;
+    if (!counts || !centroids || !bias) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!u || !topk_idx || !topk_gate || !tie_flag || !ws)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_MISALIGNED;
+    if (T == 0) return launch_route_tc(u, centroids, bias, 0, d, E, K, topk_idx, topk_gate,
+                                       tie_flag, counts, ws, nullptr, S_(stream));
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < route_ws_bytes(T, d, E)) return MOE_ERR_WORKSPACE;
+    int32_t* status = static_cast<int32_t*>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), S_(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_route_tc(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
+                           ws, status, S_(stream), n_groups, topk_groups, group_topk);
 }
 
 int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
@@ -273,7 +307,8 @@ int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, i
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if ((rc = launch_route_tc(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
-                              counts, route_ws, status, st)))
+                              counts, route_ws, status, st, L->n_groups, L->topk_groups,
+                              L->group_topk)))
         return rc;
     if (T == 0) return MOE_OK;
     if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,

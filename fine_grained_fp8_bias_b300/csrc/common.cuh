@@ -61,7 +61,8 @@ int launch_route(const uint16_t* u, const float* cent, const float* bias, int T,
 size_t route_ws_bytes(int T, int d, int E);
 int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                     int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
-                    int32_t* status, cudaStream_t st);
+                    int32_t* status, cudaStream_t st, int n_groups = 0, int topk_groups = 0,
+                    int group_topk = 0);
 // The router's logit estimates summed into out [T, E], and the bound's
 // largest centroid norm into *cmax_out (device), for checking the bound.
 int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,

@@ -481,6 +481,279 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
     if (lane == 0) tie[t] = (K < E && (zk - zk1) < 1e-6f) ? 1 : 0;
 }
 
+// ------------------------------------------------------------ 3b. grouped
+// Group-limited selection: experts form n_groups contiguous groups of gs; a
+// group's score is the float32 sum, largest first, of its group_topk best z;
+// the topk_groups best groups are kept (equal: lower group index); top-K by z
+// among their experts.  Flagged as a near tie also when the last kept and the
+// next group score differ by less than 1e-6.
+// Two exact rounds: (A) in every group whose estimated score could reach the
+// cut, the experts that could be among its best group_topk; the kept groups
+// follow from exact scores.  (B) in the kept groups, the experts within the
+// band of the K-th estimated score.  Lane g of warp 0 scans group g.
+// Shared memory: u_t [d] bf16, then zap, zex, sex [32 NV] float (estimated
+// and exact z, exact s by expert; zex is NaN until computed), and the work
+// list [32 NV] int.
+template <int NV>
+__global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
+    const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
+    const float* __restrict__ part, int split, int T, int d, int E, int K, int n_groups,
+    int topk_groups, int group_topk, const unsigned int* __restrict__ cmax_bits,
+    int32_t* __restrict__ idx, float* __restrict__ gate, uint8_t* __restrict__ tie,
+    int32_t* __restrict__ counts) {
+    extern __shared__ __align__(16) uint8_t sel_sm[];
+    __shared__ float red[SEL_WARPS];
+    __shared__ int n_work;
+    __shared__ int all_mode;
+    __shared__ int gtie_sh;
+    uint16_t* ut = reinterpret_cast<uint16_t*>(sel_sm);
+    float* zap = reinterpret_cast<float*>(sel_sm + (size_t)d * 2);
+    float* zex = zap + NV * 32;
+    float* sex = zex + NV * 32;
+    int* work = reinterpret_cast<int*>(sex + NV * 32);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    const int gs = E / n_groups;
+
+    float ss = 0.0f;
+    for (int j = threadIdx.x * 8; j < d; j += SEL_WARPS * 32 * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(u + (size_t)t * d + j);
+        *reinterpret_cast<uint4*>(ut + j) = v;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
+            const float hi = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+    }
+    for (int e = threadIdx.x; e < NV * 32; e += SEL_WARPS * 32) zex[e] = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+
+    // the best `n` values of group g in arr (NaN entries skipped), summed largest
+    // first; also returns the n-th largest
+    auto group_best = [&](const float* arr, int g, int n, float& nth) -> float {
+        float acc = 0.0f, prev = FLT_MAX;
+        int prev_e = -1;
+        nth = -FLT_MAX;
+        for (int k = 0; k < n; ++k) {
+            float best = -FLT_MAX;
+            int be = -1;
+            for (int e = g * gs; e < (g + 1) * gs; ++e) {
+                const float v = arr[e];
+                if (v != v) continue;
+                // strictly after (prev, prev_e) in the order (value desc, index asc)
+                const bool after = v < prev || (v == prev && e > prev_e);
+                if (after && (be < 0 || v > best)) { best = v; be = e; }
+            }
+            if (be < 0) break;
+            acc += best;
+            nth = best;
+            prev = best;
+            prev_e = be;
+        }
+        return acc;
+    };
+
+    float eps_z = 0.0f;
+    bool possible = false;
+    float za[NV];
+    if (warp == 0) {
+        ss = 0.0f;
+#pragma unroll
+        for (int w = 0; w < SEL_WARPS; ++w) ss += red[w];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if (e < E) {
+                float l = 0.0f;
+                for (int s = 0; s < split; ++s) l += part[((size_t)s * T + t) * E + e];
+                za[j] = sigmoid(l) + bias[e];
+                zap[e] = za[j];
+            } else {
+                za[j] = -FLT_MAX;
+            }
+        }
+        __syncwarp();
+        const float eps_l = GAMMA * sqrtf(ss) * __uint_as_float(*cmax_bits);
+        // round A: estimated group scores, the groups that could reach the cut
+        float zg = -FLT_MAX, ga = -FLT_MAX;
+        if (lane < n_groups) ga = group_best(zap, lane, group_topk, zg);
+        float gav[1] = {ga};
+        const float gaM = kth_largest(gav, n_groups, topk_groups, lane);
+        float zmax = fabsf(gaM) + 1.0f;
+        eps_z = 0.25f * eps_l + 1e-6f + 0x1p-22f * zmax;
+        const float eps_g = group_topk * eps_z + 0x1p-22f * zmax;
+        possible = lane < n_groups && ga >= gaM - 2.0f * eps_g - 2e-6f;
+        int cnt = 0;
+        if (possible)
+            for (int e = lane * gs; e < (lane + 1) * gs; ++e)
+                cnt += zap[e] >= zg - 2.0f * eps_z - 2e-6f;
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total > CAND_CAP) {
+            // too many: every expert is recomputed
+            for (int e = lane; e < E; e += 32) work[e] = e;
+            if (lane == 0) { n_work = E; all_mode = 1; }
+        } else {
+            int at = incl - cnt;
+            if (possible)
+                for (int e = lane * gs; e < (lane + 1) * gs; ++e)
+                    if (zap[e] >= zg - 2.0f * eps_z - 2e-6f) work[at++] = e;
+            if (lane == 0) { n_work = total; all_mode = 0; }
+        }
+    }
+    __syncthreads();
+    auto run_work = [&]() {
+        const int n = n_work;
+        for (int k = warp; k < n; k += SEL_WARPS) {
+            const int e = work[k];
+            const float l = exact_dot(ut, c + (size_t)e * d, d, lane);
+            if (lane == 0) {
+                const float sv = sigmoid(l);
+                sex[e] = sv;
+                zex[e] = sv + bias[e];
+            }
+        }
+    };
+    run_work();
+    __syncthreads();
+
+    unsigned keptmask = 0;
+    if (warp == 0) {
+        const bool all = all_mode != 0;
+        // exact scores of the groups in question, the kept groups, group near tie
+        float gx = -FLT_MAX, dummy;
+        if (lane < n_groups && (possible || all)) gx = group_best(zex, lane, group_topk, dummy);
+        unsigned taken = 0;
+        float gm = -FLT_MAX, gm1 = -FLT_MAX;
+        for (int k = 0; k < topk_groups + 1 && k < n_groups; ++k) {
+            float bz = (lane < n_groups && !taken) ? gx : -FLT_MAX;
+            int be = (lane < n_groups && !taken) ? lane : 0x7fffffff;
+            float wz = bz;
+            int we = be;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float oz = __shfl_xor_sync(0xffffffffu, wz, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, we, off);
+                if (better(oz, oe, wz, we)) { wz = oz; we = oe; }
+            }
+            if (k < topk_groups) {
+                if (lane == we) taken = 1;
+                keptmask |= 1u << we;
+                if (k == topk_groups - 1) gm = wz;
+            } else {
+                gm1 = wz;
+            }
+        }
+        if (lane == 0) gtie_sh = (topk_groups < n_groups && gm1 != -FLT_MAX && (gm - gm1) < 1e-6f);
+        // round B: in the kept groups, the band of the K-th estimated score
+        float zk[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            zk[j] = (e < E && (keptmask >> (e / gs) & 1u)) ? za[j] : -FLT_MAX;
+        }
+        const float zK = kth_largest(zk, E, K, lane);
+        unsigned need = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            const bool in = e < E && (keptmask >> (e / gs) & 1u);
+            const bool band = all || zk[j] >= zK - 2.0f * eps_z - 2e-6f;
+            if (in && band && zex[e] != zex[e]) need |= 1u << j;
+        }
+        int base = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const unsigned m = __ballot_sync(0xffffffffu, (need >> j) & 1u);
+            if ((need >> j) & 1u) work[base + __popc(m & ((1u << lane) - 1u))] = j * 32 + lane;
+            base += __popc(m);
+        }
+        if (lane == 0) n_work = base;
+    }
+    __syncthreads();
+    run_work();
+    __syncthreads();
+    if (warp != 0) return;
+
+    // selection among the kept groups' recomputed experts
+    float s[NV], z[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int e = j * 32 + lane;
+        const bool ok = e < E && (keptmask >> (e / gs) & 1u) && zex[e] == zex[e];
+        s[j] = ok ? sex[e] : 0.0f;
+        z[j] = ok ? zex[e] : -FLT_MAX;
+    }
+    unsigned taken = 0;
+    float my_s = 0.0f, ssum = 0.0f, zsel = 0.0f, zsel1 = -FLT_MAX;
+    int my_e = -1;
+    for (int k = 0; k < K + 1; ++k) {
+        float bz = -FLT_MAX;
+        int be = 0x7fffffff, bj = -1;
+        float bs = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if (z[j] != -FLT_MAX && !(taken >> j & 1u) && better(z[j], e, bz, be)) {
+                bz = z[j]; be = e; bj = j; bs = s[j];
+            }
+        }
+        float wz = bz, ws = bs;
+        int we = be;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, wz, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, we, off);
+            const float os = __shfl_xor_sync(0xffffffffu, ws, off);
+            if (better(oz, oe, wz, we)) { wz = oz; we = oe; ws = os; }
+        }
+        if (we == be && bj >= 0) taken |= 1u << bj;
+        if (k < K) {
+            ssum += ws;
+            if (lane == k) { my_e = we; my_s = ws; }
+            if (k == K - 1) zsel = wz;
+        } else {
+            zsel1 = wz;                                  // -FLT_MAX: nobody left
+        }
+    }
+    if (lane < K) {
+        idx[(size_t)t * K + lane] = my_e;
+        gate[(size_t)t * K + lane] = __fdiv_rn(my_s, ssum);
+        atomicAdd(&counts[my_e], 1);
+    }
+    if (lane == 0) {
+        const bool ktie = zsel1 != -FLT_MAX && (zsel - zsel1) < 1e-6f;
+        tie[t] = (ktie || gtie_sh) ? 1 : 0;
+    }
+}
+
+template <int NV>
+int launch_select_grouped(const uint16_t* u, const float* c, const float* bias, const float* part,
+                          int split, int T, int d, int E, int K, int n_groups, int topk_groups,
+                          int group_topk, const unsigned int* cmax, int32_t* idx, float* gate,
+                          uint8_t* tie, int32_t* counts, cudaStream_t st) {
+    const size_t smem = (size_t)d * 2 + (size_t)NV * 32 * 16;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(select_refine_grouped_kernel<NV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    select_refine_grouped_kernel<NV><<<T, SEL_WARPS * 32, smem, st>>>(
+        u, c, bias, part, split, T, d, E, K, n_groups, topk_groups, group_topk, cmax, idx, gate,
+        tie, counts);
+    return check_launch();
+}
+
 template <int NV>
 int launch_select(const uint16_t* u, const float* c, const float* bias, const float* part,
                   int split, int T, int d, int E, int K, const unsigned int* cmax, int32_t* idx,
@@ -563,7 +836,8 @@ int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, in
 
 int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                     int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
-                    int32_t* status, cudaStream_t st) {
+                    int32_t* status, cudaStream_t st, int n_groups, int topk_groups,
+                    int group_topk) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (e != cudaSuccess) return cuda_fail(e);
     if (T == 0) return MOE_OK;
@@ -572,6 +846,18 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
     int split, rc;
     if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &cmax))) return rc;
     const int nv = (E + 31) / 32;
+    if (n_groups > 0) {
+#define MOE_GROUPED(N)                                                                          \
+    return launch_select_grouped<N>(u, cent, bias, part, split, T, d, E, K, n_groups, topk_groups, \
+                                    group_topk, cmax, idx, gate, tie, counts, st)
+        if (nv <= 1) MOE_GROUPED(1);
+        if (nv <= 2) MOE_GROUPED(2);
+        if (nv <= 4) MOE_GROUPED(4);
+        if (nv <= 8) MOE_GROUPED(8);
+        if (nv <= 16) MOE_GROUPED(16);
+        MOE_GROUPED(32);
+#undef MOE_GROUPED
+    }
     if (nv <= 1) return launch_select<1>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
     if (nv <= 2) return launch_select<2>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
     if (nv <= 4) return launch_select<4>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);

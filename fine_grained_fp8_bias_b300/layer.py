@@ -28,6 +28,11 @@ class MoELayer:
         self.s_down = torch.ones((self.G, d // 128, I // 128), dtype=torch.float32, device=dev)
         self._ws = None
         self._T_ws = -1
+        # group-limited routing (moe_route_grouped); 0 groups: plain top-K
+        self.n_groups = self.topk_groups = self.group_topk = 0
+
+    def set_group_routing(self, n_groups: int, topk_groups: int, group_topk: int):
+        self.n_groups, self.topk_groups, self.group_topk = n_groups, topk_groups, group_topk
 
     # ------------------------------------------------------------ set-up
     @classmethod
@@ -35,6 +40,7 @@ class MoELayer:
         """Synthetic layer of a workload: seeded centroids, bias and master
         weights, each weight matrix quantised 128x128 by moe_quant_128x128."""
         L = cls(cfg.d, cfg.E, cfg.K, cfg.S, cfg.I, device)
+        L.set_group_routing(cfg.n_groups, cfg.topk_groups, cfg.group_topk)
         L.centroids.copy_(workloads.centroids(cfg, L.device))
         L.bias.copy_(workloads.bias(cfg, L.device))
         for g in range(L.G):
@@ -56,7 +62,8 @@ class MoELayer:
                                self.centroids.data_ptr(), self.bias.data_ptr(),
                                self.w_gate.data_ptr(), self.w_up.data_ptr(),
                                self.w_down.data_ptr(), self.s_gate.data_ptr(),
-                               self.s_up.data_ptr(), self.s_down.data_ptr())
+                               self.s_up.data_ptr(), self.s_down.data_ptr(),
+                               self.n_groups, self.topk_groups, self.group_topk)
 
     def workspace(self, T: int) -> torch.Tensor:
         if self._ws is None or self._T_ws < T:

@@ -37,7 +37,8 @@ class MoeError(RuntimeError):
 class moe_layer_t(ctypes.Structure):
     _fields_ = [("d", I32), ("E", I32), ("K", I32), ("S", I32), ("I", I32),
                 ("centroids", P), ("bias", P), ("w_gate", P), ("w_up", P), ("w_down", P),
-                ("s_gate", P), ("s_up", P), ("s_down", P)]
+                ("s_gate", P), ("s_up", P), ("s_down", P),
+                ("n_groups", I32), ("topk_groups", I32), ("group_topk", I32)]
 
 
 class moe_batch_buffers_t(ctypes.Structure):
@@ -68,6 +69,8 @@ def _load() -> ctypes.CDLL:
         "moe_quant_1x128_dispatch": [P, I32, I32, P, I32, I32, P, P, I32, P, P],
         "moe_route": [P, P, P, I32, I32, I32, I32, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_route_noalloc": [P, P, P, I32, I32, I32, I32, P, P, P, P, P],
+        "moe_route_grouped": [P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
+                              ctypes.c_size_t, P],
         "moe_route_estimate_logits": [P, P, I32, I32, I32, P, P, P, ctypes.c_size_t, P],
         "moe_permute": [P, I32, I32, I32, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_grouped_gemm_fp8": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
@@ -204,6 +207,33 @@ def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: i
     _check(_lib.moe_route(_ptr(u), _ptr(centroids), _ptr(bias), T, d, E, K, _ptr(out["idx"]),
                           _ptr(out["gate"]), _ptr(out["tie"]), _ptr(out["counts"]), _ptr(ws),
                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+    return out
+
+
+def moe_route_grouped(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
+                      n_groups: int, topk_groups: int, group_topk: int,
+                      ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+                      stream=None) -> dict:
+    """Group-limited routing: keep the topk_groups best of n_groups expert
+    groups (score: sum of a group's group_topk best biased scores), then top-K
+    inside them."""
+    _bits(u, torch.bfloat16)
+    _dev(u, "u")
+    T, d = u.shape
+    E = centroids.shape[0]
+    dev = u.device
+    if out is None:
+        out = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),
+               "gate": torch.empty((T, K), dtype=torch.float32, device=dev),
+               "tie": torch.empty((T,), dtype=torch.uint8, device=dev),
+               "counts": torch.empty((E,), dtype=torch.int32, device=dev)}
+    if ws is None:
+        ws = torch.empty(route_workspace_bytes(T, E, d), dtype=torch.uint8, device=dev)
+    _check(_lib.moe_route_grouped(_ptr(u), _ptr(centroids), _ptr(bias), T, d, E, K, n_groups,
+                                  topk_groups, group_topk, _ptr(out["idx"]), _ptr(out["gate"]),
+                                  _ptr(out["tie"]), _ptr(out["counts"]), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_route_grouped")
     return out
 
 

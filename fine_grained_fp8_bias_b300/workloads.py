@@ -149,6 +149,9 @@ class LayerConfig:
     gamma: float = 1e-3
     hot_experts: int = 0        # decode skew: number of hot experts (0 = none)
     hot_alpha: float = 0.0      # decode skew: centroid shift along the calibration mean direction
+    n_groups: int = 0           # group-limited routing: expert groups (0 = plain top-K)
+    topk_groups: int = 0        # groups kept per token
+    group_topk: int = 0         # best scores summed into a group's score
 
     @property
     def G(self) -> int:
@@ -166,11 +169,15 @@ V3_DECODE = LayerConfig("v3_decode", T=256, d=7168, E=256, K=8, S=1, I=2048, see
 V3_LONG = LayerConfig("v3_long", T=32768, d=7168, E=256, K=8, S=1, I=2048, seed=4,
                       tokens="mixture4")
 
+# The V3 prefill batch with node-limited routing: 8 groups of 32 experts (one
+# per node), at most 4 groups per token, group score from its 2 best experts.
+V3_GROUPED = V3_PREFILL.with_(name="v3_grouped", n_groups=8, topk_groups=4, group_topk=2)
+
 # Profiling-size slice of the V3 prefill batch: the same expert shapes and the
 # same rows per expert (T*K/E = 128), 32 routed experts (1.45 GB of weights).
 V3_SLICE = LayerConfig("v3_slice", T=512, d=7168, E=32, K=8, S=1, I=2048, seed=5)
 
-CONFIGS = {c.name: c for c in (TINY, MID, V3_PREFILL, V3_DECODE, V3_LONG, V3_SLICE)}
+CONFIGS = {c.name: c for c in (TINY, MID, V3_PREFILL, V3_DECODE, V3_LONG, V3_SLICE, V3_GROUPED)}
 
 
 def tokens(cfg: LayerConfig, device="cpu", step: int = 0) -> torch.Tensor:

@@ -72,6 +72,8 @@ typedef struct moe_layer_t {
     const float* s_gate;      /* [E+S, I/128, d/128] block scales                     */
     const float* s_up;        /* [E+S, I/128, d/128]                                  */
     const float* s_down;      /* [E+S, d/128, I/128]                                  */
+    /* Group-limited routing (moe_route_grouped); n_groups = 0: plain top-K.  */
+    int n_groups, topk_groups, group_topk;
 } moe_layer_t;
 
 /* Text of a status code (static storage; never NULL). */
@@ -141,6 +143,24 @@ int moe_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, v
 int moe_route(const uint16_t* u, const float* centroids, const float* bias, int T, int d, int E,
               int K, int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
               void* ws, size_t ws_bytes, void* stream);
+
+/* Group-limited routing.  The pages say only that a token is sent to at most
+ * M = 4 nodes ([YLY] §2.2; [SYH], table of innovations); the scoring is this
+ * library's reading: the E experts form n_groups contiguous groups of
+ * E / n_groups (one per node); a group's score is the float32 sum, largest
+ * first, of its group_topk largest biased scores s + b; the topk_groups
+ * groups with the largest scores are kept (equal: lower group index); then
+ * the top K by s + b among the kept groups' experts, gates and counts as in
+ * moe_route.  tie_flag is also 1 when the last kept and the next group score
+ * differ by less than 1e-6.  1 <= n_groups <= 32, n_groups divides E,
+ * 1 <= topk_groups <= n_groups, 1 <= group_topk <= E / n_groups,
+ * K <= topk_groups * E / n_groups.  Same logits, workspace and status word as
+ * moe_route (the experts whose scores the group choice or the selection
+ * depend on are recomputed exactly). */
+int moe_route_grouped(const uint16_t* u, const float* centroids, const float* bias, int T, int d,
+                      int E, int K, int n_groups, int topk_groups, int group_topk,
+                      int32_t* topk_idx, float* topk_gate, uint8_t* tie_flag, int32_t* counts,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* Workspace bytes moe_route needs for T tokens, hidden size d and E experts
  * (0 for invalid sizes). */
@@ -233,7 +253,8 @@ int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
 /* The whole layer forward: route, dispatch, quantise, GEMM (gate/up + SiLU),
  * GEMM (down), combine -- all enqueued on `stream` with no host sync.
  * Outputs: h_out [T, d] float32 and the routing (topk_idx, topk_gate,
- * counts, tie_flag as in moe_route), which moe_update_bias consumes.
+ * counts, tie_flag as in moe_route, or moe_route_grouped when L->n_groups >
+ * 0), which moe_update_bias consumes.
  * ws: at least moe_workspace_size(L, T) bytes, 256-byte aligned.  Its first
  * 16 bytes hold the device status word of this call (read it with
  * moe_check_device_status(ws, stream)). */
