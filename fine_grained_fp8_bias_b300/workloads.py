@@ -173,11 +173,16 @@ V3_LONG = LayerConfig("v3_long", T=32768, d=7168, E=256, K=8, S=1, I=2048, seed=
 # per node), at most 4 groups per token, group score from its 2 best experts.
 V3_GROUPED = V3_PREFILL.with_(name="v3_grouped", n_groups=8, topk_groups=4, group_topk=2)
 
+# The V3 prefill batch with skewed expert popularity: 16 hot experts whose
+# centroids lean towards the tokens' mean direction (as the decode workload).
+V3_SKEW = V3_PREFILL.with_(name="v3_skew", hot_experts=16, hot_alpha=0.5)
+
 # Profiling-size slice of the V3 prefill batch: the same expert shapes and the
 # same rows per expert (T*K/E = 128), 32 routed experts (1.45 GB of weights).
 V3_SLICE = LayerConfig("v3_slice", T=512, d=7168, E=32, K=8, S=1, I=2048, seed=5)
 
-CONFIGS = {c.name: c for c in (TINY, MID, V3_PREFILL, V3_DECODE, V3_LONG, V3_SLICE, V3_GROUPED)}
+CONFIGS = {c.name: c for c in (TINY, MID, V3_PREFILL, V3_DECODE, V3_LONG, V3_SLICE, V3_GROUPED,
+                                V3_SKEW)}
 
 
 def tokens(cfg: LayerConfig, device="cpu", step: int = 0) -> torch.Tensor:
