@@ -376,27 +376,42 @@ def run_e2e(layer, cfg, dev, steps, world):
                    "overlapped across steps)"}
 
 
-def run_decode(layer, cfg, dev, pk, T=64, steps=50):
-    """Decode-sized batch on the same V3 weights: forward time and the HBM rate of
-    the weights it touches (distinct experts + shared)."""
-    dcfg = wl.V3_DECODE.with_(T=T)
-    u = wl.tokens(dcfg, dev)
-    out = layer.outputs(T)
-    for _ in range(5):
-        layer.forward(u, out)
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        layer.forward(u, out)
-    e.record()
-    torch.cuda.synchronize()
-    us = s.elapsed_time(e) / steps * 1e3
-    touched = int((out["counts"].cpu() > 0).sum()) + cfg.S
-    wbytes = touched * 3 * cfg.d * cfg.I * (1 + 4 / 128 ** 2)
-    return {"T": T, "us_per_forward": round(us, 1), "experts_touched": touched,
-            "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
-            "frac_of_hbm": round(wbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4)}
+def run_decode(layer, cfg, dev, pk, Ts=(1, 16, 64, 256), steps=50):
+    """Decode-sized batches on the V3 weights with the skewed decode routing
+    (centroids and bias of the decode workload: 16 hot experts take 40% of the
+    selections at T = 256): forward time and the HBM rate of the weights each
+    forward touches (distinct experts + shared)."""
+    dcfg = wl.V3_DECODE
+    saved_c, saved_b = layer.centroids.clone(), layer.bias.clone()
+    layer.centroids.copy_(wl.centroids(dcfg, dev))
+    layer.bias.copy_(wl.bias(dcfg, dev))
+    res = []
+    try:
+        for T in Ts:
+            u = wl.tokens(dcfg.with_(T=T), dev)
+            out = layer.outputs(T)
+            for _ in range(5):
+                layer.forward(u, out)
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(steps):
+                layer.forward(u, out)
+            e.record()
+            torch.cuda.synchronize()
+            us = s.elapsed_time(e) / steps * 1e3
+            counts = out["counts"].cpu()
+            touched = int((counts > 0).sum()) + cfg.S
+            wbytes = touched * 3 * cfg.d * cfg.I * (1 + 4 / 128 ** 2)
+            hot = float(counts[:dcfg.hot_experts].sum()) / (T * cfg.K)
+            res.append({"T": T, "us_per_forward": round(us, 1), "experts_touched": touched,
+                        "hot_fraction": round(hot, 3),
+                        "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
+                        "frac_of_hbm": round(wbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4)})
+    finally:
+        layer.centroids.copy_(saved_c)
+        layer.bias.copy_(saved_b)
+    return res
 
 
 def run_balance(layer, cfg, dev, steps=100):

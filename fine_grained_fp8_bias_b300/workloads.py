@@ -164,8 +164,12 @@ class LayerConfig:
 TINY = LayerConfig("tiny", T=256, d=256, E=16, K=2, S=1, I=128, seed=0)
 MID = LayerConfig("mid", T=4096, d=2048, E=64, K=6, S=2, I=1408, seed=1, bias="zeros")
 V3_PREFILL = LayerConfig("v3_prefill", T=4096, d=7168, E=256, K=8, S=1, I=2048, seed=2)
+# hot_alpha: the shift that gives the 16 hot experts 40% of the selections of
+# the T = 256 batch under the oracle's routing (bisection by
+# tests/golden/calibrate_decode_skew.py, recorded in tests/golden/decode_skew.json).
+DECODE_HOT_ALPHA = 5.25
 V3_DECODE = LayerConfig("v3_decode", T=256, d=7168, E=256, K=8, S=1, I=2048, seed=3,
-                        hot_experts=16, hot_alpha=0.5)
+                        hot_experts=16, hot_alpha=DECODE_HOT_ALPHA)
 V3_LONG = LayerConfig("v3_long", T=32768, d=7168, E=256, K=8, S=1, I=2048, seed=4,
                       tokens="mixture4")
 
@@ -175,7 +179,7 @@ V3_GROUPED = V3_PREFILL.with_(name="v3_grouped", n_groups=8, topk_groups=4, grou
 
 # The V3 prefill batch with skewed expert popularity: 16 hot experts whose
 # centroids lean towards the tokens' mean direction (as the decode workload).
-V3_SKEW = V3_PREFILL.with_(name="v3_skew", hot_experts=16, hot_alpha=0.5)
+V3_SKEW = V3_PREFILL.with_(name="v3_skew", hot_experts=16, hot_alpha=DECODE_HOT_ALPHA)
 
 # Profiling-size slice of the V3 prefill batch: the same expert shapes and the
 # same rows per expert (T*K/E = 128), 32 routed experts (1.45 GB of weights).

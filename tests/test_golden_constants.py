@@ -45,3 +45,13 @@ def test_generator_is_deterministic_and_has_the_requested_moments():
     assert np.array_equal(full[500:800].numpy(), part.numpy())
     u = wl.uniform(wl.stream_key(3, 4), (100000,), -0.05, 0.05)
     assert u.min() >= -0.05 and u.max() < 0.05
+
+
+def test_decode_skew_is_the_calibrated_one():
+    # the workload's hot-expert shift is the one the calibration script found
+    import json
+    import os
+    from fine_grained_fp8_bias_b300 import workloads as wl
+    rec = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "decode_skew.json")))
+    assert wl.V3_DECODE.hot_alpha == rec["hot_alpha"]
+    assert abs(rec["hot_fraction_T256"] - rec["target"]) <= rec["tolerance"]
