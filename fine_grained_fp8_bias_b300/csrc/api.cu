@@ -156,19 +156,19 @@ size_t moe_route_workspace_size(int T, int d, int E) {
 }
 
 int moe_route_estimate_logits(const uint16_t* u, const float* centroids, int T, int d, int E,
-                              float* logits, float* cmax, void* ws, size_t ws_bytes,
+                              float* logits, float* norms, void* ws, size_t ws_bytes,
                               void* stream) {
     if (T < 0 || d <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
     if (d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;
-    if (!u || !centroids || !logits || !cmax || !ws) return MOE_ERR_INVALID_ARG;
+    if (!u || !centroids || !logits || !norms || !ws) return MOE_ERR_INVALID_ARG;
     if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_MISALIGNED;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
     if (ws_bytes < route_ws_bytes(T, d, E)) return MOE_ERR_WORKSPACE;
     int32_t* status = static_cast<int32_t*>(ws);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), S_(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    return launch_route_estimate(u, centroids, T, d, E, logits, cmax, ws, status, S_(stream));
+    return launch_route_estimate(u, centroids, T, d, E, logits, norms, ws, status, S_(stream));
 }
 
 int moe_route_grouped(const uint16_t* u, const float* centroids, const float* bias, int T, int d,

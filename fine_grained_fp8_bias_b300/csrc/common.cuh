@@ -64,9 +64,9 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
                     int32_t* status, cudaStream_t st, int n_groups = 0, int topk_groups = 0,
                     int group_topk = 0);
 // The router's logit estimates summed into out [T, E], and the bound's
-// largest centroid norm into *cmax_out (device), for checking the bound.
+// centroid norms of the bound into norms_out [E] (device), for checking the bound.
 int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,
-                          float* cmax_out, void* ws, int32_t* status, cudaStream_t st);
+                          float* norms_out, void* ws, int32_t* status, cudaStream_t st);
 int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);

@@ -16,17 +16,18 @@
 //   2. logits_tc: l~ = u hi^T + u mid^T on the tensor cores
 //      (tcgen05.mma.kind::f16, bf16 operands, float32 accumulation in TMEM),
 //      split over d when there are few token tiles; partial sums to [split][T][E].
-//   3. select_refine, one warp per token: the approximate biased scores
-//      z~ = sigmoid(l~) + b give the K-th largest z~_K.  |l~ - l| is bounded by
-//      gamma |u_t| max_e |c_e| (gamma = 2^-11 covers the split remainder and an
-//      error of one float32 ulp of the running sum per MMA instruction, with
-//      twofold headroom), and sigmoid has slope at most 1/4, which bounds
-//      |z~ - z| by eps.  Every expert with z~ >= z~_K - 2 eps - 2e-6 is a
-//      candidate: no other expert can be selected or lie within 2e-6 of the
-//      K-th score.  The candidates' logits are recomputed on CUDA cores with
-//      compensated summation (32-term FMA chains added with TwoSum), and the
-//      selection, gates and tie flag use those.  A token with more than 32
-//      candidates (degenerate inputs: many equal scores) recomputes all E.
+//   3. select_refine, one block per token: |l~_e - l_e| is bounded by
+//      gamma |u_t| |c_e| (gamma = 2^-11 covers the split remainder and an error
+//      of one float32 ulp of the running sum per MMA instruction, with twofold
+//      headroom), and sigmoid has slope at most 1/4, so every biased score z_e
+//      lies in [lo_e, hi_e] around its estimate.  The K-th largest z is at
+//      least L_K, the K-th largest lo; an expert with hi_e < L_K - 2e-6 can
+//      neither be selected nor lie within 2e-6 of the K-th score, and every
+//      other expert is a candidate.  The candidates' logits are recomputed on
+//      CUDA cores with compensated summation (32-term FMA chains added with
+//      TwoSum), and the selection, gates and tie flag use those.  A token with
+//      more than 64 candidates (degenerate inputs: many equal scores)
+//      recomputes all E.
 // Selection order: descending s + b, equal scores broken by the lower expert
 // index.  Near-tie flag: the K-th and (K+1)-th biased scores differ by less
 // than 1e-6.
@@ -48,7 +49,7 @@ constexpr int RT_SMEM_B = RT_N * RT_K * 2;          // 16 KB per centroid piece
 constexpr int RT_STAGE = RT_SMEM_A + 2 * RT_SMEM_B; // 48 KB
 constexpr int RT_THREADS = 128;
 constexpr uint32_t RT_TMEM_COLS = 128;
-constexpr int CAND_CAP = 32;
+constexpr int CAND_CAP = 64;
 constexpr float GAMMA = 0x1p-11f;
 constexpr int SEL_WARPS = 4;                        // warps per token in select_refine
 
@@ -61,9 +62,9 @@ struct RtCtl {
 };
 constexpr size_t RT_SMEM_BYTES = 1024 + (size_t)RT_STAGES * RT_STAGE + sizeof(RtCtl);
 
-// Workspace: header (status word, largest centroid norm), hi, mid, partial logits.
+// Workspace: header (status word), centroid norms, hi, mid, partial logits.
 struct RouteWs {
-    size_t status, cmax, hi, mid, part, total;
+    size_t status, norms, hi, mid, part, total;
     int split;
 };
 
@@ -79,8 +80,8 @@ RouteWs route_ws(int T, int d, int E) {
     RouteWs w{};
     w.split = route_split(T, E, d);
     w.status = 0;
-    w.cmax = 16;
-    w.hi = 256;
+    w.norms = 256;
+    w.hi = align_up(w.norms + sizeof(float) * (size_t)E, 256);
     w.mid = align_up(w.hi + (size_t)E * d * 2, 256);
     w.part = align_up(w.mid + (size_t)E * d * 2, 256);
     w.total = align_up(w.part + sizeof(float) * (size_t)w.split * T * E, 256);
@@ -103,13 +104,12 @@ __device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
 }
 
 // ------------------------------------------------------------ 1. split
-// One block per expert row: hi/mid pieces and |c_e|; the largest norm (times
-// 1 + 2^-20 for its own rounding) goes to *cmax_bits with an integer max,
-// which orders non-negative floats correctly.
+// One block per expert row: hi/mid pieces and |c_e| (times 1 + 2^-20 for its
+// own rounding) to norms[e].
 constexpr int SPLIT_THREADS = 256;
 __global__ void __launch_bounds__(SPLIT_THREADS) split_centroids_kernel(
     const float* __restrict__ c, int E, int d, uint16_t* __restrict__ hi,
-    uint16_t* __restrict__ mid, unsigned int* __restrict__ cmax_bits) {
+    uint16_t* __restrict__ mid, float* __restrict__ norms) {
     __shared__ float wsum[SPLIT_THREADS / 32];
     const int e = blockIdx.x;
     float ss = 0.0f;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) split_centroids_kernel(
     if (threadIdx.x == 0) {
         float t = 0.0f;
         for (int w = 0; w < SPLIT_THREADS / 32; ++w) t += wsum[w];
-        atomicMax(cmax_bits, __float_as_uint(sqrtf(t) * (1.0f + 0x1p-20f)));
+        norms[e] = sqrtf(t) * (1.0f + 0x1p-20f);
     }
 }
 
@@ -339,7 +339,7 @@ template <int NV>
 __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
     const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
     const float* __restrict__ part, int split, int T, int d, int E, int K,
-    const unsigned int* __restrict__ cmax_bits, int32_t* __restrict__ idx, float* __restrict__ gate,
+    const float* __restrict__ norms, int32_t* __restrict__ idx, float* __restrict__ gate,
     uint8_t* __restrict__ tie, int32_t* __restrict__ counts) {
     extern __shared__ __align__(16) uint8_t sel_sm[];
     __shared__ float red[SEL_WARPS];
@@ -386,14 +386,25 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
                 za[j] = -FLT_MAX;
             }
         }
-        const float zk_approx = kth_largest(za, E, K, lane);
-        const float eps_l = GAMMA * sqrtf(ss) * __uint_as_float(*cmax_bits);
-        const float eps_z = 0.25f * eps_l + 1e-6f + 0x1p-22f * (fabsf(zk_approx) + 1.0f);
-        const float thr = zk_approx - 2.0f * eps_z - 2e-6f;
+        // per-expert bounds [lo, hi] of the biased scores
+        const float gu = GAMMA * sqrtf(ss);
+        float lo[NV], hi[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = j * 32 + lane;
+            if (e < E) {
+                const float eps = 0.25f * gu * norms[e] + 1e-6f + 0x1p-22f * (fabsf(za[j]) + 1.0f);
+                lo[j] = za[j] - eps;
+                hi[j] = za[j] + eps;
+            } else {
+                lo[j] = hi[j] = -FLT_MAX;
+            }
+        }
+        const float LK = kth_largest(lo, E, K, lane);
         unsigned cand = 0;
 #pragma unroll
         for (int j = 0; j < NV; ++j)
-            if (j * 32 + lane < E && za[j] >= thr) cand |= 1u << j;
+            if (j * 32 + lane < E && hi[j] >= LK - 2e-6f) cand |= 1u << j;
         int n = __popc(cand);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
@@ -491,14 +502,16 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
 // cut, the experts that could be among its best group_topk; the kept groups
 // follow from exact scores.  (B) in the kept groups, the experts within the
 // band of the K-th estimated score.  Lane g of warp 0 scans group g.
-// Shared memory: u_t [d] bf16, then zap, zex, sex [32 NV] float (estimated
-// and exact z, exact s by expert; zex is NaN until computed), and the work
-// list [32 NV] int.
+// Shared memory: u_t [d] bf16, then zlo, zhi, zex, sex [32 NV] float (bounds
+// of z around its estimate, exact z and s by expert; zex is NaN until
+// computed), and the work list [32 NV] int.  A group's score lies between the
+// sum of its group_topk largest lower bounds and that of its group_topk
+// largest upper bounds.
 template <int NV>
 __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
     const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
     const float* __restrict__ part, int split, int T, int d, int E, int K, int n_groups,
-    int topk_groups, int group_topk, const unsigned int* __restrict__ cmax_bits,
+    int topk_groups, int group_topk, const float* __restrict__ norms,
     int32_t* __restrict__ idx, float* __restrict__ gate, uint8_t* __restrict__ tie,
     int32_t* __restrict__ counts) {
     extern __shared__ __align__(16) uint8_t sel_sm[];
@@ -507,8 +520,9 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
     __shared__ int all_mode;
     __shared__ int gtie_sh;
     uint16_t* ut = reinterpret_cast<uint16_t*>(sel_sm);
-    float* zap = reinterpret_cast<float*>(sel_sm + (size_t)d * 2);
-    float* zex = zap + NV * 32;
+    float* zlo = reinterpret_cast<float*>(sel_sm + (size_t)d * 2);
+    float* zhi = zlo + NV * 32;
+    float* zex = zhi + NV * 32;
     float* sex = zex + NV * 32;
     int* work = reinterpret_cast<int*>(sex + NV * 32);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -558,9 +572,8 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
         return acc;
     };
 
-    float eps_z = 0.0f;
     bool possible = false;
-    float za[NV];
+    float za[NV], lo[NV], hi[NV];
     if (warp == 0) {
         ss = 0.0f;
 #pragma unroll
@@ -572,26 +585,33 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
                 float l = 0.0f;
                 for (int s = 0; s < split; ++s) l += part[((size_t)s * T + t) * E + e];
                 za[j] = sigmoid(l) + bias[e];
-                zap[e] = za[j];
+                const float eps = 0.25f * GAMMA * sqrtf(ss) * norms[e] + 1e-6f +
+                                  0x1p-22f * (fabsf(za[j]) + 1.0f);
+                lo[j] = za[j] - eps;
+                hi[j] = za[j] + eps;
+                zlo[e] = lo[j];
+                zhi[e] = hi[j];
             } else {
-                za[j] = -FLT_MAX;
+                za[j] = lo[j] = hi[j] = -FLT_MAX;
             }
         }
         __syncwarp();
-        const float eps_l = GAMMA * sqrtf(ss) * __uint_as_float(*cmax_bits);
-        // round A: estimated group scores, the groups that could reach the cut
-        float zg = -FLT_MAX, ga = -FLT_MAX;
-        if (lane < n_groups) ga = group_best(zap, lane, group_topk, zg);
-        float gav[1] = {ga};
-        const float gaM = kth_largest(gav, n_groups, topk_groups, lane);
-        float zmax = fabsf(gaM) + 1.0f;
-        eps_z = 0.25f * eps_l + 1e-6f + 0x1p-22f * zmax;
-        const float eps_g = group_topk * eps_z + 0x1p-22f * zmax;
-        possible = lane < n_groups && ga >= gaM - 2.0f * eps_g - 2e-6f;
+        // round A: bounds of the group scores, the groups that could reach the cut
+        float lg = -FLT_MAX, Lg = -FLT_MAX, ug = -FLT_MAX, dummy;
+        if (lane < n_groups) {
+            lg = group_best(zlo, lane, group_topk, Lg);
+            ug = group_best(zhi, lane, group_topk, dummy);
+            ug += 0x1p-22f * group_topk * (fabsf(ug) + 1.0f);     // float32 rounding of the sums
+            lg -= 0x1p-22f * group_topk * (fabsf(lg) + 1.0f);
+        }
+        float lgv[1] = {lg};
+        const float LM = kth_largest(lgv, n_groups, topk_groups, lane);
+        possible = lane < n_groups && ug >= LM - 2e-6f;
+        // in a possible group, the experts that could be among its best group_topk
         int cnt = 0;
         if (possible)
             for (int e = lane * gs; e < (lane + 1) * gs; ++e)
-                cnt += zap[e] >= zg - 2.0f * eps_z - 2e-6f;
+                cnt += zhi[e] >= Lg;
         int incl = cnt;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -607,7 +627,7 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
             int at = incl - cnt;
             if (possible)
                 for (int e = lane * gs; e < (lane + 1) * gs; ++e)
-                    if (zap[e] >= zg - 2.0f * eps_z - 2e-6f) work[at++] = e;
+                    if (zhi[e] >= Lg) work[at++] = e;
             if (lane == 0) { n_work = total; all_mode = 0; }
         }
     }
@@ -655,20 +675,21 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
             }
         }
         if (lane == 0) gtie_sh = (topk_groups < n_groups && gm1 != -FLT_MAX && (gm - gm1) < 1e-6f);
-        // round B: in the kept groups, the band of the K-th estimated score
+        // round B: in the kept groups, every expert whose upper bound reaches the
+        // K-th largest lower bound (less the tie band)
         float zk[NV];
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int e = j * 32 + lane;
-            zk[j] = (e < E && (keptmask >> (e / gs) & 1u)) ? za[j] : -FLT_MAX;
+            zk[j] = (e < E && (keptmask >> (e / gs) & 1u)) ? lo[j] : -FLT_MAX;
         }
-        const float zK = kth_largest(zk, E, K, lane);
+        const float LK = kth_largest(zk, E, K, lane);
         unsigned need = 0;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int e = j * 32 + lane;
             const bool in = e < E && (keptmask >> (e / gs) & 1u);
-            const bool band = all || zk[j] >= zK - 2.0f * eps_z - 2e-6f;
+            const bool band = all || hi[j] >= LK - 2e-6f;
             if (in && band && zex[e] != zex[e]) need |= 1u << j;
         }
         int base = 0;
@@ -740,23 +761,23 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
 template <int NV>
 int launch_select_grouped(const uint16_t* u, const float* c, const float* bias, const float* part,
                           int split, int T, int d, int E, int K, int n_groups, int topk_groups,
-                          int group_topk, const unsigned int* cmax, int32_t* idx, float* gate,
+                          int group_topk, const float* norms, int32_t* idx, float* gate,
                           uint8_t* tie, int32_t* counts, cudaStream_t st) {
-    const size_t smem = (size_t)d * 2 + (size_t)NV * 32 * 16;
+    const size_t smem = (size_t)d * 2 + (size_t)NV * 32 * 20;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_refine_grouped_kernel<NV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     select_refine_grouped_kernel<NV><<<T, SEL_WARPS * 32, smem, st>>>(
-        u, c, bias, part, split, T, d, E, K, n_groups, topk_groups, group_topk, cmax, idx, gate,
+        u, c, bias, part, split, T, d, E, K, n_groups, topk_groups, group_topk, norms, idx, gate,
         tie, counts);
     return check_launch();
 }
 
 template <int NV>
 int launch_select(const uint16_t* u, const float* c, const float* bias, const float* part,
-                  int split, int T, int d, int E, int K, const unsigned int* cmax, int32_t* idx,
+                  int split, int T, int d, int E, int K, const float* norms, int32_t* idx,
                   float* gate, uint8_t* tie, int32_t* counts, cudaStream_t st) {
     const size_t smem = (size_t)d * 2 + (size_t)NV * 32 * 12;
     if (smem > 48 * 1024) {
@@ -765,7 +786,7 @@ int launch_select(const uint16_t* u, const float* c, const float* bias, const fl
         if (e != cudaSuccess) return cuda_fail(e);
     }
     select_refine_kernel<NV><<<T, SEL_WARPS * 32, smem, st>>>(u, c, bias, part, split, T, d, E, K,
-                                                             cmax, idx, gate, tie, counts);
+                                                             norms, idx, gate, tie, counts);
     return check_launch();
 }
 
@@ -779,25 +800,24 @@ __global__ void sum_partials_kernel(const float* __restrict__ part, int split, s
     }
 }
 
-// Steps 1 and 2 of the router; returns the partial-sum array.
+// Steps 1 and 2 of the router: the centroid pieces and norms, and the
+// partial logit estimates.
 int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, void* ws,
                     int32_t* status, cudaStream_t st, const float** part_out, int* split_out,
-                    const unsigned int** cmax_out) {
+                    const float** norms_out) {
     const RouteWs W = route_ws(T, d, E);
     char* base = static_cast<char*>(ws);
-    unsigned int* cmax = reinterpret_cast<unsigned int*>(base + W.cmax);
+    float* norms = reinterpret_cast<float*>(base + W.norms);
     uint16_t* hi = reinterpret_cast<uint16_t*>(base + W.hi);
     uint16_t* mid = reinterpret_cast<uint16_t*>(base + W.mid);
     float* part = reinterpret_cast<float*>(base + W.part);
-    cudaError_t e = cudaMemsetAsync(cmax, 0, sizeof(unsigned int), st);
-    if (e != cudaSuccess) return cuda_fail(e);
     int rc;
-    split_centroids_kernel<<<E, SPLIT_THREADS, 0, st>>>(cent, E, d, hi, mid, cmax);
+    split_centroids_kernel<<<E, SPLIT_THREADS, 0, st>>>(cent, E, d, hi, mid, norms);
     if ((rc = check_launch())) return rc;
     static bool attr_set = false;
     if (!attr_set) {
-        e = cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)RT_SMEM_BYTES);
+        const cudaError_t e = cudaFuncSetAttribute(
+            logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RT_SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
         attr_set = true;
     }
@@ -811,7 +831,7 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
     if ((rc = check_launch())) return rc;
     *part_out = part;
     *split_out = W.split;
-    *cmax_out = cmax;
+    *norms_out = norms;
     return MOE_OK;
 }
 
@@ -820,17 +840,18 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
 size_t route_ws_bytes(int T, int d, int E) { return route_ws(T, d, E).total; }
 
 int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,
-                          float* cmax_out, void* ws, int32_t* status, cudaStream_t st) {
+                          float* norms_out, void* ws, int32_t* status, cudaStream_t st) {
     if (T == 0) return MOE_OK;
     const float* part;
-    const unsigned int* cmax;
+    const float* norms;
     int split, rc;
-    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &cmax))) return rc;
+    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &norms))) return rc;
     const size_t n = (size_t)T * E;
     sum_partials_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(
         part, split, n, out);
     if ((rc = check_launch())) return rc;
-    const cudaError_t e = cudaMemcpyAsync(cmax_out, cmax, sizeof(float), cudaMemcpyDeviceToDevice, st);
+    const cudaError_t e = cudaMemcpyAsync(norms_out, norms, sizeof(float) * (size_t)E,
+                                          cudaMemcpyDeviceToDevice, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
@@ -842,14 +863,14 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
     if (e != cudaSuccess) return cuda_fail(e);
     if (T == 0) return MOE_OK;
     const float* part;
-    const unsigned int* cmax;
+    const float* norms;
     int split, rc;
-    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &cmax))) return rc;
+    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &norms))) return rc;
     const int nv = (E + 31) / 32;
     if (n_groups > 0) {
 #define MOE_GROUPED(N)                                                                          \
     return launch_select_grouped<N>(u, cent, bias, part, split, T, d, E, K, n_groups, topk_groups, \
-                                    group_topk, cmax, idx, gate, tie, counts, st)
+                                    group_topk, norms, idx, gate, tie, counts, st)
         if (nv <= 1) MOE_GROUPED(1);
         if (nv <= 2) MOE_GROUPED(2);
         if (nv <= 4) MOE_GROUPED(4);
@@ -858,12 +879,12 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
         MOE_GROUPED(32);
 #undef MOE_GROUPED
     }
-    if (nv <= 1) return launch_select<1>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
-    if (nv <= 2) return launch_select<2>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
-    if (nv <= 4) return launch_select<4>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
-    if (nv <= 8) return launch_select<8>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
-    if (nv <= 16) return launch_select<16>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
-    return launch_select<32>(u, cent, bias, part, split, T, d, E, K, cmax, idx, gate, tie, counts, st);
+    if (nv <= 1) return launch_select<1>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
+    if (nv <= 2) return launch_select<2>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
+    if (nv <= 4) return launch_select<4>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
+    if (nv <= 8) return launch_select<8>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
+    if (nv <= 16) return launch_select<16>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
+    return launch_select<32>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
 }
 
 }  // namespace moe

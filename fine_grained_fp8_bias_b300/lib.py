@@ -238,19 +238,19 @@ def moe_route_grouped(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tens
 
 
 def moe_route_estimate_logits(u: torch.Tensor, centroids: torch.Tensor, stream=None):
-    """The router's tensor-core logit estimates [T, E] and the largest centroid
-    norm of its error bound (check hook of moe_route's screening step)."""
+    """The router's tensor-core logit estimates [T, E] and the per-expert
+    centroid norms of its error bound (check hook of moe_route's screening step)."""
     _bits(u, torch.bfloat16)
     _dev(u, "u")
     T, d = u.shape
     E = centroids.shape[0]
     out = torch.empty((T, E), dtype=torch.float32, device=u.device)
-    cmax = torch.empty((1,), dtype=torch.float32, device=u.device)
+    norms = torch.empty((E,), dtype=torch.float32, device=u.device)
     ws = torch.empty(route_workspace_bytes(T, E, d), dtype=torch.uint8, device=u.device)
-    _check(_lib.moe_route_estimate_logits(_ptr(u), _ptr(centroids), T, d, E, _ptr(out), _ptr(cmax),
+    _check(_lib.moe_route_estimate_logits(_ptr(u), _ptr(centroids), T, d, E, _ptr(out), _ptr(norms),
                                           _ptr(ws), ws.numel(), _stream(stream)),
            "moe_route_estimate_logits")
-    return out, cmax
+    return out, norms
 
 
 def moe_route_noalloc(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,

@@ -168,11 +168,11 @@ size_t moe_route_workspace_size(int T, int d, int E);
 
 /* Check hook for moe_route's screening step (no counterpart in the pages):
  * writes the tensor-core logit estimates l~ [T, E] float32 to logits and the
- * largest centroid norm (as used in the error bound) to cmax [1] float32,
- * both device memory.  moe_route treats |l~ - l| <= 2^-11 |u_t| cmax as the
+ * centroid norms used in the error bound to norms [E] float32, both device
+ * memory.  moe_route treats |l~_e - l_e| <= 2^-11 |u_t| norms[e] as the
  * estimate's error bound.  Same workspace rules as moe_route. */
 int moe_route_estimate_logits(const uint16_t* u, const float* centroids, int T, int d, int E,
-                              float* logits, float* cmax, void* ws, size_t ws_bytes,
+                              float* logits, float* norms, void* ws, size_t ws_bytes,
                               void* stream);
 
 /* moe_route without a workspace, for callers that cannot allocate device

@@ -22,6 +22,7 @@ CASES = {
     "v3_small": wl.V3_GROUPED.with_(T=300),
     "odd": wl.LayerConfig("odd", T=77, d=384, E=96, K=5, S=0, I=128, seed=61, n_groups=12,
                           topk_groups=3, group_topk=3),
+    "v3_skew": wl.V3_SKEW.with_(T=300, n_groups=8, topk_groups=4, group_topk=2),
 }
 
 
