@@ -379,8 +379,9 @@ def run_e2e(layer, cfg, dev, steps, world):
 def run_decode(layer, cfg, dev, pk, Ts=(1, 16, 64, 256), steps=50):
     """Decode-sized batches on the V3 weights with the skewed decode routing
     (centroids and bias of the decode workload: 16 hot experts take 40% of the
-    selections at T = 256): forward time and the HBM rate of the weights each
-    forward touches (distinct experts + shared)."""
+    selections at T = 256), each step a replay of a CUDA graph of moe_forward:
+    forward time and the HBM rate of the weights each forward touches
+    (distinct experts + shared)."""
     dcfg = wl.V3_DECODE
     saved_c, saved_b = layer.centroids.clone(), layer.bias.clone()
     layer.centroids.copy_(wl.centroids(dcfg, dev))
@@ -389,16 +390,19 @@ def run_decode(layer, cfg, dev, pk, Ts=(1, 16, 64, 256), steps=50):
     try:
         for T in Ts:
             u = wl.tokens(dcfg.with_(T=T), dev)
-            out = layer.outputs(T)
+            # one decode step = one replay of the captured moe_forward
+            graph, out = layer.capture_forward(u)
             for _ in range(5):
-                layer.forward(u, out)
+                graph.replay()
             torch.cuda.synchronize()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
             for _ in range(steps):
-                layer.forward(u, out)
+                graph.replay()
             e.record()
             torch.cuda.synchronize()
+            if layer.status() != 0:
+                raise RuntimeError("device status flagged in the decode leg")
             us = s.elapsed_time(e) / steps * 1e3
             counts = out["counts"].cpu()
             touched = int((counts > 0).sum()) + cfg.S

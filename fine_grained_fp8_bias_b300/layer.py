@@ -112,6 +112,25 @@ class MoELayer:
                              *streams)
         return bufs
 
+    def capture_forward(self, u: torch.Tensor, out: dict | None = None):
+        """A CUDA graph of moe_forward on the fixed buffers u and out (decode
+        steps: the launches of one forward become one graph launch).  Refill u
+        in place and call .replay(); out holds the results.  Returns
+        (graph, out)."""
+        T = u.shape[0]
+        out = self.outputs(T) if out is None else out
+        ws = self.workspace(T)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            for _ in range(2):                       # first-call set-up outside the capture
+                lib.moe_forward(self.struct(), u, ws, out, side)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            lib.moe_forward(self.struct(), u, ws, out, side)
+        return g, out
+
     def update_bias(self, counts: torch.Tensor, T: int, gamma: float, stream=None):
         lib.moe_update_bias(counts, self.bias, T, self.K, gamma, stream)
 
