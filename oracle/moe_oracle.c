@@ -48,6 +48,8 @@
  *   R10 bias update: with n = T*K selections, expert e is overloaded when
  *       c_e * E > n and underloaded when c_e * E < n (integer compare);
  *       b_e -= gamma or += gamma in float32; equal load leaves b_e unchanged.
+ *   R15 input gradient of the layer: the backward GEMMs follow the
+ *       forward's FP8 rule (see orc_layer_backward_dgrad).
  *   R14 group-limited routing (the pages: a token goes to at most M = 4
  *       nodes, no scoring rule given): experts form n_groups contiguous
  *       groups; group score = float32 sum, largest first, of the group's
@@ -476,6 +478,156 @@ void orc_layer_forward(const uint16_t* u, int T, int d, int E, int K, int S, int
         for (int j = 0; j < d; ++j) out[(int64_t)n * d + j] = (float)h[j];
     }
     free(qa); free(sa); free(y); free(h);
+}
+
+/* ------------------------------------------------------------------ */
+/* Input gradient of the layer (R15).  The pages say only that FP8       */
+/* carries the inputs and part of the gradient propagation while master  */
+/* weights and gradients stay in 16/32 bits ("DeepSeek V3技術報告", FP8   */
+/* 資料格式訓練), and ask for transposed-GEMM support in hardware          */
+/* ("官方揭秘DeepSeek-V3模型训练全流程", hardware suggestions).  Reading: */
+/* every expert backward GEMM follows the forward's FP8 rule -- operand   */
+/* rows quantised per 1x128 tile, weights as their 128x128 blocks (W^T    */
+/* uses the same codes and block scales, transposed), promotion per 128:  */
+/*   dy = g_k dh (routed; float32 product) or dh (shared), quantised;     */
+/*   dH = bf16(dy W_down)                    (W_down^T as the B operand); */
+/*   G, U recomputed as in the forward; sigma = 1 / (1 + exp(-G));         */
+/*   dG = dH U sigma (1 + G (1 - sigma)), dU = dH G sigma (float32);      */
+/*   [dG | dU] quantised per 1x128 tile along 2I;                          */
+/*   dA = bf16([dG | dU] [W_gate ; W_up])    (contraction over 2I);        */
+/*   du = dh + sum_shared dA + sum_routed dA                               */
+/*        + sum_k dl_k e_k, with dg_k = dh . y_k (y_k the forward's       */
+/*        bf16 expert output), ds_k = (dg_k - sum_j g_j dg_j) / sum_j s_j, */
+/*        dl_k = ds_k s_k (1 - s_k)  (the gates' dependence on u through  */
+/*        s = sigmoid(u . e); the bias has no gradient).                   */
+/* ------------------------------------------------------------------ */
+
+/* float32 -> bfloat16 (round to nearest even) -> float32 */
+static float bf16_round(float x) {
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    if ((b & 0x7f800000u) == 0x7f800000u) return x;
+    b += 0x7fffu + ((b >> 16) & 1u);
+    b &= 0xffff0000u;
+    float y;
+    memcpy(&y, &b, 4);
+    return y;
+}
+
+/* W [R, C] codes with block scales [R/128, C/128] -> W^T [C, R], [C/128, R/128] */
+static void transpose_blocks(const uint8_t* q, const float* s, int R, int C, uint8_t* qt,
+                             float* st) {
+    for (int r = 0; r < R; ++r)
+        for (int c = 0; c < C; ++c) qt[(int64_t)c * R + r] = q[(int64_t)r * C + c];
+    for (int i = 0; i < R / 128; ++i)
+        for (int j = 0; j < C / 128; ++j) st[(int64_t)j * (R / 128) + i] = s[(int64_t)i * (C / 128) + j];
+}
+
+/* du [n_tok, d] float32 for the listed tokens; dh [T, d] bf16 upstream
+ * gradient of h'; idx, gate [T, K] the forward's routing; cent [E, d]. */
+void orc_layer_backward_dgrad(const uint16_t* u, int T, int d, int E, int K, int S, int I,
+                              const float* cent, const int32_t* idx, const float* gate,
+                              const uint8_t* const* wg, const float* const* sg,
+                              const uint8_t* const* wu, const float* const* su,
+                              const uint8_t* const* wd, const float* const* sd,
+                              const uint16_t* dh, const int32_t* tok, int n_tok, float* du) {
+    (void)T;
+    uint8_t* qa = (uint8_t*)malloc((size_t)d);
+    float* sa = (float*)malloc(sizeof(float) * (size_t)(d / 128));
+    float* G = (float*)malloc(sizeof(float) * (size_t)I);
+    float* U = (float*)malloc(sizeof(float) * (size_t)I);
+    float* h = (float*)malloc(sizeof(float) * (size_t)I);
+    uint8_t* qh = (uint8_t*)malloc((size_t)I);
+    float* sh = (float*)malloc(sizeof(float) * (size_t)(I / 128));
+    float* y = (float*)malloc(sizeof(float) * (size_t)d);
+    float* dy = (float*)malloc(sizeof(float) * (size_t)d);
+    uint8_t* qdy = (uint8_t*)malloc((size_t)d);
+    float* sdy = (float*)malloc(sizeof(float) * (size_t)(d / 128));
+    float* dH = (float*)malloc(sizeof(float) * (size_t)I);
+    float* dgu = (float*)malloc(sizeof(float) * (size_t)2 * I);
+    uint8_t* qgu = (uint8_t*)malloc((size_t)2 * I);
+    float* sgu = (float*)malloc(sizeof(float) * (size_t)(2 * I / 128));
+    float* dA = (float*)malloc(sizeof(float) * (size_t)d);
+    float* dhf = (float*)malloc(sizeof(float) * (size_t)d);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dg = (double*)malloc(sizeof(double) * (size_t)K);
+    uint8_t* wdT = (uint8_t*)malloc((size_t)I * d);
+    float* sdT = (float*)malloc(sizeof(float) * (size_t)(I / 128) * (d / 128));
+    uint8_t* wguT = (uint8_t*)malloc((size_t)d * 2 * I);
+    float* sguT = (float*)malloc(sizeof(float) * (size_t)(d / 128) * (2 * I / 128));
+    uint8_t* tq = (uint8_t*)malloc((size_t)d * I);
+    float* ts = (float*)malloc(sizeof(float) * (size_t)(d / 128) * (I / 128));
+    const int nI = I / 128, nd = d / 128;
+    for (int n = 0; n < n_tok; ++n) {
+        const int t = tok[n];
+        const uint16_t* ut = u + (int64_t)t * d;
+        orc_quant_1x128_bf16(ut, 1, d, qa, sa);
+        for (int j = 0; j < d; ++j) {
+            dhf[j] = bf16_to_f32(dh[(int64_t)t * d + j]);
+            acc[j] = (double)dhf[j];
+        }
+        for (int q = 0; q < S + K; ++q) {
+            const int shared = q < S;
+            const int g = shared ? E + q : idx[(int64_t)t * K + (q - S)];
+            const float gk = shared ? 1.0f : gate[(int64_t)t * K + (q - S)];
+            /* the forward pieces, recomputed */
+            orc_gemm_fp8(qa, sa, 1, d, wg[g], sg[g], I, G);
+            orc_gemm_fp8(qa, sa, 1, d, wu[g], su[g], I, U);
+            for (int i = 0; i < I; ++i) h[i] = G[i] / (1.0f + expf(-G[i])) * U[i];
+            orc_quant_1x128_f32(h, 1, I, qh, sh);
+            orc_gemm_fp8(qh, sh, 1, I, wd[g], sd[g], d, y);
+            /* gradient of the expert output, quantised per 1x128 tile */
+            for (int j = 0; j < d; ++j) dy[j] = shared ? dhf[j] : gk * dhf[j];
+            orc_quant_1x128_f32(dy, 1, d, qdy, sdy);
+            /* dH = dy W_down (B operand W_down^T [I, d]) */
+            transpose_blocks(wd[g], sd[g], d, I, wdT, sdT);
+            orc_gemm_fp8(qdy, sdy, 1, d, wdT, sdT, I, dH);
+            for (int i = 0; i < I; ++i) dH[i] = bf16_round(dH[i]);
+            /* SiLU backward */
+            for (int i = 0; i < I; ++i) {
+                const float sgm = 1.0f / (1.0f + expf(-G[i]));
+                dgu[i] = dH[i] * U[i] * sgm * (1.0f + G[i] * (1.0f - sgm));
+                dgu[I + i] = dH[i] * G[i] * sgm;
+            }
+            orc_quant_1x128_f32(dgu, 1, 2 * I, qgu, sgu);
+            /* dA = [dG | dU] [W_gate ; W_up]: B operand [W_gate^T | W_up^T] [d, 2I] */
+            transpose_blocks(wg[g], sg[g], I, d, tq, ts);
+            for (int r = 0; r < d; ++r) memcpy(wguT + (int64_t)r * 2 * I, tq + (int64_t)r * I, (size_t)I);
+            for (int i = 0; i < nd; ++i) memcpy(sguT + (int64_t)i * 2 * nI, ts + (int64_t)i * nI, sizeof(float) * nI);
+            transpose_blocks(wu[g], su[g], I, d, tq, ts);
+            for (int r = 0; r < d; ++r) memcpy(wguT + (int64_t)r * 2 * I + I, tq + (int64_t)r * I, (size_t)I);
+            for (int i = 0; i < nd; ++i) memcpy(sguT + (int64_t)i * 2 * nI + nI, ts + (int64_t)i * nI, sizeof(float) * nI);
+            orc_gemm_fp8(qgu, sgu, 1, 2 * I, wguT, sguT, d, dA);
+            for (int j = 0; j < d; ++j) acc[j] += (double)bf16_round(dA[j]);
+            if (!shared) {
+                double s_ = 0.0;
+                for (int j = 0; j < d; ++j) s_ += (double)dhf[j] * (double)bf16_round(y[j]);
+                dg[q - S] = s_;
+            }
+        }
+        /* the gates' dependence on u through s = sigmoid(u . e) */
+        double ssum = 0.0, gdg = 0.0;
+        double* sk = (double*)malloc(sizeof(double) * (size_t)K);
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[(int64_t)t * K + k];
+            double l = 0.0;
+            for (int j = 0; j < d; ++j) l += (double)bf16_to_f32(ut[j]) * (double)cent[(int64_t)e * d + j];
+            const float lf = (float)l;
+            sk[k] = (double)(float)(1.0 / (1.0 + exp(-(double)lf)));
+            ssum += sk[k];
+            gdg += (double)gate[(int64_t)t * K + k] * dg[k];
+        }
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[(int64_t)t * K + k];
+            const double dl = (dg[k] - gdg) / ssum * sk[k] * (1.0 - sk[k]);
+            for (int j = 0; j < d; ++j) acc[j] += dl * (double)cent[(int64_t)e * d + j];
+        }
+        free(sk);
+        for (int j = 0; j < d; ++j) du[(int64_t)n * d + j] = (float)acc[j];
+    }
+    free(qa); free(sa); free(G); free(U); free(h); free(qh); free(sh); free(y); free(dy);
+    free(qdy); free(sdy); free(dH); free(dgu); free(qgu); free(sgu); free(dA); free(dhf);
+    free(acc); free(dg); free(wdT); free(sdT); free(wguT); free(sguT); free(tq); free(ts);
 }
 
 /* ------------------------------------------------------------------ */

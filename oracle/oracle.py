@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         _lib.orc_layer_forward.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P,
                                            P, P, P, P, P, P, P, i32, P]
         _lib.orc_update_bias.argtypes = [P, i32, i32, i32, ctypes.c_float, P]
+        _lib.orc_layer_backward_dgrad.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P,
+                                                  P, P, P, P, P, P, P, P, i32, P]
     return _lib
 
 
@@ -239,6 +241,33 @@ def route_grouped(u_bits, cent, bias, K: int, n_groups: int, topk_groups: int,
     lib().orc_route_grouped(_p(u_bits), _p(cent), _p(bias), T, d, E, K, n_groups, topk_groups,
                             group_topk, _p(idx), _p(gate), _p(tie), _p(counts), _p(scores))
     return {"idx": idx, "gate": gate, "tie": tie, "counts": counts, "scores": scores}
+
+
+def layer_backward_dgrad(u_bits, idx, gate, W: Weights, cent, dh_bits, d: int, E: int, K: int,
+                         S: int, I: int, tokens: Sequence[int]) -> np.ndarray:
+    """du for the listed tokens (reading R15) -> float32 [len(tokens), d].
+    dh_bits: bfloat16 bit patterns [T, d] of the upstream gradient of h'."""
+    u_bits, dh_bits = _c(u_bits, np.uint16), _c(dh_bits, np.uint16)
+    idx, gate, cent = _c(idx, np.int32), _c(gate, np.float32), _c(cent, np.float32)
+    T = u_bits.shape[0]
+    tok = _c(tokens, np.int32)
+    G = E + S
+    for t in tok:
+        for g in list(idx[t]) + list(range(E, G)):
+            if W.gate[g] is None:
+                raise ValueError(f"weights of group {g} are needed for token {t}")
+
+    def ptrs(lst, j):
+        arr = (ctypes.c_void_p * G)()
+        for g in range(G):
+            arr[g] = lst[g][j].ctypes.data if lst[g] is not None else None
+        return arr
+    out = np.empty((len(tok), d), np.float32)
+    lib().orc_layer_backward_dgrad(_p(u_bits), T, d, E, K, S, I, _p(cent), _p(idx), _p(gate),
+                                   ptrs(W.gate, 0), ptrs(W.gate, 1), ptrs(W.up, 0), ptrs(W.up, 1),
+                                   ptrs(W.down, 0), ptrs(W.down, 1), _p(dh_bits), _p(tok),
+                                   len(tok), _p(out))
+    return out
 
 
 def update_bias(counts, bias, T: int, K: int, gamma: float) -> np.ndarray:
