@@ -324,6 +324,32 @@ int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, i
     return launch_combine(u, Y, topk_gate, inv_row, Y + (size_t)T * K * d, T, d, K, S, h_out, st);
 }
 
+// Backward workspace: status, dy codes and scales, dH, [dG | dU] codes and
+// scales, dA.
+struct BwdLayout {
+    size_t status, dyq, sdy, dH, dgu, sgu, dA, total;
+};
+
+BwdLayout bwd_layout(int T, int d, int K, int S, int I) {
+    BwdLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    const size_t M = (size_t)T * (K + S);
+    L.status = take(16);
+    L.dyq = take(M * d);
+    L.sdy = take(sizeof(float) * M * (d / 128));
+    L.dH = take(sizeof(uint16_t) * M * I);
+    L.dgu = take(M * 2 * I);
+    L.sgu = take(sizeof(float) * M * (2 * I / 128));
+    L.dA = take(sizeof(uint16_t) * M * d);
+    L.total = off;
+    return L;
+}
+
 struct EventSet {
     cudaEvent_t ev[6] = {};
     ~EventSet() {
@@ -342,6 +368,89 @@ int moe_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, in
                 void* stream) {
     return forward_impl(L, u, T, h_out, topk_idx, topk_gate, counts, tie_flag, ws, ws_bytes,
                         S_(stream), true);
+}
+
+size_t moe_backward_workspace_size(const moe_layer_t* L, int T_max) {
+    if (check_layer(L) || T_max < 0) return 0;
+    return bwd_layout(T_max, L->d, L->K, L->S, L->I).total;
+}
+
+int moe_prepare_backward_weights(const moe_layer_t* L, uint8_t* w_down_t, float* s_down_t,
+                                 uint8_t* w_gu_t, float* s_gu_t, void* stream) {
+    int rc = check_layer(L);
+    if (rc) return rc;
+    if (!w_down_t || !s_down_t || !w_gu_t || !s_gu_t) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_down_t) || !aligned16(w_gu_t)) return MOE_ERR_MISALIGNED;
+    const int G = L->E + L->S, d = L->d, I = L->I;
+    const cudaStream_t st = S_(stream);
+    // W_down [G, d, I] -> W_down^T [G, I, d]
+    if ((rc = launch_transpose_blocks(L->w_down, L->s_down, G, d, I, w_down_t, d, 0, s_down_t,
+                                      d / 128, 0, st)))
+        return rc;
+    // W_gate, W_up [G, I, d] -> [W_gate^T | W_up^T] [G, d, 2I]
+    if ((rc = launch_transpose_blocks(L->w_gate, L->s_gate, G, I, d, w_gu_t, 2 * I, 0, s_gu_t,
+                                      2 * I / 128, 0, st)))
+        return rc;
+    return launch_transpose_blocks(L->w_up, L->s_up, G, I, d, w_gu_t, 2 * I, I, s_gu_t, 2 * I / 128,
+                                   I / 128, st);
+}
+
+int moe_backward_dgrad(const moe_layer_t* L, const moe_layer_bwd_t* B, const uint16_t* u,
+                       const uint16_t* dh, int T, const int32_t* topk_idx, const float* topk_gate,
+                       float* du, void* fwd_ws, size_t fwd_ws_bytes, void* bwd_ws,
+                       size_t bwd_ws_bytes, void* stream) {
+    int rc = check_layer(L);
+    if (rc) return rc;
+    if (!B || !B->w_down_t || !B->s_down_t || !B->w_gu_t || !B->s_gu_t) return MOE_ERR_INVALID_ARG;
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!u || !dh || !topk_idx || !topk_gate || !du || !fwd_ws || !bwd_ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(dh) || !aligned16(du) || !aligned16(B->w_down_t) ||
+        !aligned16(B->w_gu_t))
+        return MOE_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(fwd_ws) | reinterpret_cast<uintptr_t>(bwd_ws)) & 255u)
+        return MOE_ERR_MISALIGNED;
+    if ((long long)T * (L->K + L->S) > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int d = L->d, E = L->E, K = L->K, S = L->S, I = L->I, G = E + S;
+    const Layout W = layout(T, d, E, K, S, I);
+    const BwdLayout BW = bwd_layout(T, d, K, S, I);
+    if (fwd_ws_bytes < W.total || bwd_ws_bytes < BW.total) return MOE_ERR_WORKSPACE;
+    char* fb = static_cast<char*>(fwd_ws);
+    char* bb = static_cast<char*>(bwd_ws);
+    const cudaStream_t st = S_(stream);
+    int32_t* status = reinterpret_cast<int32_t*>(bb + BW.status);
+    const int32_t* go = reinterpret_cast<const int32_t*>(fb + W.go);
+    const int32_t* inv_row = reinterpret_cast<const int32_t*>(fb + W.inv_row);
+    const uint8_t* A = reinterpret_cast<const uint8_t*>(fb + W.A);
+    const float* sa = reinterpret_cast<const float*>(fb + W.sa);
+    const uint16_t* Y = reinterpret_cast<const uint16_t*>(fb + W.Y);
+    uint8_t* dyq = reinterpret_cast<uint8_t*>(bb + BW.dyq);
+    float* sdy = reinterpret_cast<float*>(bb + BW.sdy);
+    uint16_t* dH = reinterpret_cast<uint16_t*>(bb + BW.dH);
+    uint8_t* dgu = reinterpret_cast<uint8_t*>(bb + BW.dgu);
+    float* sgu = reinterpret_cast<float*>(bb + BW.sgu);
+    uint16_t* dA = reinterpret_cast<uint16_t*>(bb + BW.dA);
+    const int M = T * (K + S);
+    cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((rc = launch_quant_dy(dh, T, d, topk_gate, inv_row, K, S, dyq, sdy, M, status, st))) return rc;
+    // dH = dy W_down
+    if ((rc = launch_grouped_gemm(MOE_GEMM_DOWN, dyq, sdy, M, go, G, B->w_down_t, nullptr,
+                                  B->s_down_t, nullptr, I, d, dH, nullptr, status, st)))
+        return rc;
+    // G, U recomputed; [dG | dU]
+    if ((rc = launch_grouped_gemm(MOE_GEMM_GATE_UP_DGRAD, A, sa, M, go, G, L->w_gate, L->w_up,
+                                  L->s_gate, L->s_up, I, d, dgu, sgu, status, st, dH)))
+        return rc;
+    // dA = [dG | dU] [W_gate ; W_up]
+    if ((rc = launch_grouped_gemm(MOE_GEMM_DOWN, dgu, sgu, M, go, G, B->w_gu_t, nullptr, B->s_gu_t,
+                                  nullptr, d, 2 * I, dA, nullptr, status, st)))
+        return rc;
+    // du = dh + sum of the token's rows of dA, then the gate term
+    if ((rc = launch_combine(dh, dA, nullptr, inv_row, dA + (size_t)T * K * d, T, d, K, S, du, st)))
+        return rc;
+    return launch_gate_term(u, dh, Y, inv_row, topk_idx, topk_gate, L->centroids, T, d, K, M, du,
+                            status, st);
 }
 
 int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t* const* u_host,

@@ -19,7 +19,8 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], uint4 raw, float w) 
 }
 
 // One block per token (grid-stride); each thread owns 8 consecutive columns
-// per step.  Sum order: u, shared experts, routed experts by slot.
+// per step.  Sum order: u, shared experts, routed experts by slot.  gate NULL:
+// every routed row has weight 1 (the input gradient's gather).
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ u,
                                                       const uint16_t* __restrict__ Y,
                                                       const float* __restrict__ gate,
@@ -33,7 +34,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
         __syncthreads();
         if (threadIdx.x < K) {
             rows[threadIdx.x] = inv_row[(size_t)t * K + threadIdx.x];
-            gs[threadIdx.x] = gate[(size_t)t * K + threadIdx.x];
+            gs[threadIdx.x] = gate ? gate[(size_t)t * K + threadIdx.x] : 1.0f;
         }
         __syncthreads();
         for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {

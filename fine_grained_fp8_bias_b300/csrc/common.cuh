@@ -67,13 +67,24 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
 // centroid norms of the bound into norms_out [E] (device), for checking the bound.
 int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,
                           float* norms_out, void* ws, int32_t* status, cudaStream_t st);
+// Input gradient of the layer (backward.cu, route_tc.cu).
+int launch_transpose_blocks(const uint8_t* src, const float* ssrc, int G, int R, int C, uint8_t* dst,
+                            int dst_ld, int col_off, float* sdst, int sdst_ld, int scol_off,
+                            cudaStream_t st);
+int launch_quant_dy(const uint16_t* dh, int T, int d, const float* gate, const int32_t* inv_row,
+                    int K, int S, uint8_t* q, float* scales, int scale_ld, int32_t* status,
+                    cudaStream_t st);
+int launch_gate_term(const uint16_t* u, const uint16_t* dh, const uint16_t* Y, const int32_t* inv_row,
+                     const int32_t* idx, const float* gate, const float* cent, int T, int d, int K,
+                     int M, float* du, int32_t* status, cudaStream_t st);
 int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);
 int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
                         const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                         const float* sw0, const float* sw1, int N, int Kdim, void* out,
-                        float* out_scales, int32_t* status, cudaStream_t st);
+                        float* out_scales, int32_t* status, cudaStream_t st,
+                        const uint16_t* dH = nullptr);
 int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
                    const uint16_t* Ysh, int T, int d, int K, int S, float* h, cudaStream_t st);
 int launch_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,

@@ -93,6 +93,7 @@ struct alignas(16) Ctl {
     int total_tiles;
     int pad;
     float amax_x[2][2][BM];                     // [tile parity][warpgroup][row]
+    float amax_y[2][2][BM];                     // second block of a row (gate/up gradient mode)
     ScaleSlot scales[SCALE_SLOTS];
     int go[kMaxGroups + 1];                     // group row offsets
     int tile_start[kMaxGroups + 1];             // first tile of each group
@@ -114,6 +115,7 @@ struct Params {
     float* out_scales;
     int32_t* status;
     int* counter;                               // next unclaimed tile (nullable: static order)
+    const uint16_t* dH;                         // gradient of h [M_total, N] bf16 (gradient mode)
 };
 
 // ----------------------------------------------------------- tile lookup
@@ -173,7 +175,10 @@ __device__ __forceinline__ bool warp_take_tile(Ctl* ctl, uint32_t& tpos, int& ti
 }
 
 // ---------------------------------------------------------------- kernel
-template <bool GATE_UP>
+// MODE 0: down projection; 1: gate/up + SiLU + re-quantisation; 2: gate/up
+// recomputed for the input gradient (SiLU backward against dH, [dG | dU]
+// re-quantised).
+template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB0,
@@ -185,7 +190,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr bool gate_up = GATE_UP;
+    constexpr bool gate_up = MODE != 0;
+    constexpr bool dgrad = MODE == 2;
     const int NT = gate_up ? p.N / 128 : (p.N + BN - 1) / BN;
     const int NB = p.N / 128;
     const int KB = p.Kdim / BK;
@@ -517,15 +523,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             // ---- tile finalisation
             if constexpr (gate_up) {
-                float amax = 0.0f;
+                float amax = 0.0f, amax2 = 0.0f;
                 if (warp_active) {
-                    // h = SiLU(g) * u with SiLU(g) = g / (1 + e^-g)
+                    if constexpr (!dgrad) {
+                        // h = SiLU(g) * u with SiLU(g) = g / (1 + e^-g)
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const float gv = acc[i];
-                        const float h = __fdiv_rn(gv, 1.0f + expf(-gv)) * acc[64 + i];
-                        acc[i] = h;
-                        amax = fmaxf(amax, fabsf(h));
+                        for (int i = 0; i < 64; ++i) {
+                            const float gv = acc[i];
+                            const float h = __fdiv_rn(gv, 1.0f + expf(-gv)) * acc[64 + i];
+                            acc[i] = h;
+                            amax = fmaxf(amax, fabsf(h));
+                        }
+                    } else {
+                        // sigma = 1 / (1 + e^-g); dG = dH u sigma (1 + g (1 - sigma)),
+                        // dU = dH g sigma; acc[0, 64) becomes dG, acc[64, 128) dU
+                        const uint16_t* dhr = p.dH + (size_t)(valid ? grow : 0) * p.N + tl.nt * 128 + wg * 64;
+#pragma unroll
+                        for (int j = 0; j < 64; j += 8) {
+                            const uint4 v = valid ? *reinterpret_cast<const uint4*>(dhr + j)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float dh = bf16_bits_to_float(static_cast<uint16_t>(
+                                    (q & 1) ? (w4[q >> 1] >> 16) : (w4[q >> 1] & 0xFFFFu)));
+                                const float gv = acc[j + q], uv = acc[64 + j + q];
+                                const float sg = __fdiv_rn(1.0f, 1.0f + expf(-gv));
+                                const float dG = dh * uv * sg * (1.0f + gv * (1.0f - sg));
+                                const float dU = dh * gv * sg;
+                                acc[j + q] = dG;
+                                acc[64 + j + q] = dU;
+                                amax = fmaxf(amax, fabsf(dG));
+                                amax2 = fmaxf(amax2, fabsf(dU));
+                            }
+                        }
                     }
                 }
                 // Exchange the row's amax with the other warpgroup.  One xbar phase per
@@ -533,36 +564,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // and the double-buffered slots keep tile n's values until then.
                 const int par = tcount & 1;
                 ctl->amax_x[par][wg][row] = amax;
+                if constexpr (dgrad) ctl->amax_y[par][wg][row] = amax2;
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->xbar);
                 if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status)) { ok = false; break; }
                 amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
-                const float scale = tile_scale(amax);
-                // a tile scale below 2^-100 (amax below ~2^-91) takes IEEE division
-                const bool fast_div = scale >= 0x1p-100f;
-                const float rs = __frcp_rn(scale);
-                if (valid) {
-                    uint8_t* dst = static_cast<uint8_t*>(p.out) + (size_t)grow * p.N + tl.nt * 128 + wg * 64;
+                if constexpr (dgrad) amax2 = fmaxf(ctl->amax_y[par][0][row], ctl->amax_y[par][1][row]);
+                // GATE_UP: one 1x128 block of h (columns 128 nt ..); gradient mode: the
+                // block of dG (columns 128 nt .. of [dG | dU]) and that of dU (N + 128 nt ..)
+                const int out_ld = dgrad ? 2 * p.N : p.N;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 16) {
-                        uint4 o;
-                        if (amax == 0.0f) {
-                            o = make_uint4(0u, 0u, 0u, 0u);
-                        } else if (!fast_div) {
-                            o.x = quant4(acc[j + 0], acc[j + 1], acc[j + 2], acc[j + 3], scale);
-                            o.y = quant4(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7], scale);
-                            o.z = quant4(acc[j + 8], acc[j + 9], acc[j + 10], acc[j + 11], scale);
-                            o.w = quant4(acc[j + 12], acc[j + 13], acc[j + 14], acc[j + 15], scale);
-                        } else {
-                            o.x = quant4_rcp(acc[j + 0], acc[j + 1], acc[j + 2], acc[j + 3], scale, rs);
-                            o.y = quant4_rcp(acc[j + 4], acc[j + 5], acc[j + 6], acc[j + 7], scale, rs);
-                            o.z = quant4_rcp(acc[j + 8], acc[j + 9], acc[j + 10], acc[j + 11], scale, rs);
-                            o.w = quant4_rcp(acc[j + 12], acc[j + 13], acc[j + 14], acc[j + 15], scale, rs);
+                for (int half = 0; half < (dgrad ? 2 : 1); ++half) {
+                    const float am = half ? amax2 : amax;
+                    const float scale = tile_scale(am);
+                    // a tile scale below 2^-100 (amax below ~2^-91) takes IEEE division
+                    const bool fast_div = scale >= 0x1p-100f;
+                    const float rs = __frcp_rn(scale);
+                    if (valid) {
+                        uint8_t* dst = static_cast<uint8_t*>(p.out) + (size_t)grow * out_ld + half * p.N +
+                                       tl.nt * 128 + wg * 64;
+#pragma unroll
+                        for (int j = 0; j < 64; j += 16) {
+                            const float* v = acc + half * 64 + j;
+                            uint4 o;
+                            if (am == 0.0f) {
+                                o = make_uint4(0u, 0u, 0u, 0u);
+                            } else if (!fast_div) {
+                                o.x = quant4(v[0], v[1], v[2], v[3], scale);
+                                o.y = quant4(v[4], v[5], v[6], v[7], scale);
+                                o.z = quant4(v[8], v[9], v[10], v[11], scale);
+                                o.w = quant4(v[12], v[13], v[14], v[15], scale);
+                            } else {
+                                o.x = quant4_rcp(v[0], v[1], v[2], v[3], scale, rs);
+                                o.y = quant4_rcp(v[4], v[5], v[6], v[7], scale, rs);
+                                o.z = quant4_rcp(v[8], v[9], v[10], v[11], scale, rs);
+                                o.w = quant4_rcp(v[12], v[13], v[14], v[15], scale, rs);
+                            }
+                            *reinterpret_cast<uint4*>(dst + j) = o;
                         }
-                        *reinterpret_cast<uint4*>(dst + j) = o;
+                        if (wg == 0)
+                            p.out_scales[(size_t)(half * NB + tl.nt) * p.M_total + grow] = scale;
                     }
-                    if (wg == 0) p.out_scales[(size_t)tl.nt * p.M_total + grow] = scale;
                 }
             } else if (valid && cols_valid) {
                 uint16_t* dst = static_cast<uint16_t*>(p.out) + (size_t)grow * p.N + tl.nt * BN + wg * 128;
@@ -595,37 +638,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
                         const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                         const float* sw0, const float* sw1, int N, int Kdim, void* out,
-                        float* out_scales, int32_t* status, cudaStream_t st) {
+                        float* out_scales, int32_t* status, cudaStream_t st, const uint16_t* dH) {
     if (M_total == 0 || G == 0) return MOE_OK;
     static int sm_count = 0;
     static std::once_flag once;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    static int num_regs[2] = {0, 0};
+    static int num_regs[3] = {0, 0, 0};
     std::call_once(once, [&] {
         cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<true>,
+        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<0>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<false>,
+        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        cudaFuncSetAttribute(grouped_gemm_fp8_kernel<2>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<true>) == cudaSuccess)
-            num_regs[1] = fa.numRegs;
-        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<false>) == cudaSuccess)
+        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<0>) == cudaSuccess)
             num_regs[0] = fa.numRegs;
+        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<1>) == cudaSuccess)
+            num_regs[1] = fa.numRegs;
+        if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel<2>) == cudaSuccess)
+            num_regs[2] = fa.numRegs;
     });
     if (sm_count <= 0) return cuda_fail(cudaErrorInvalidDevice);
     // The warpgroups re-split the registers the CTA is launched with; launching
     // with fewer than LAUNCH_REGS per thread would leave setmaxnreg.inc waiting.
-    const bool gu = mode == MOE_GEMM_GATE_UP_SILU_QUANT;
-    if (num_regs[gu ? 1 : 0] != LAUNCH_REGS) return cuda_fail(cudaErrorInvalidConfiguration);
+    const int kmode = mode == MOE_GEMM_DOWN ? 0 : (mode == MOE_GEMM_GATE_UP_SILU_QUANT ? 1 : 2);
+    const bool gu = kmode != 0;
+    if (num_regs[kmode] != LAUNCH_REGS) return cuda_fail(cudaErrorInvalidConfiguration);
     CUtensorMap mA, mB0, mB1;
     int rc = make_map_2d(&mA, A, (uint64_t)M_total, (uint64_t)Kdim, 1, 128, 128);
     if (rc) return rc;
     rc = make_map_2d(&mB0, W0, (uint64_t)G * N, (uint64_t)Kdim, 1, 128, 128);
     if (rc) return rc;
-    if (mode == MOE_GEMM_GATE_UP_SILU_QUANT) {
+    if (gu) {
         rc = make_map_2d(&mB1, W1, (uint64_t)G * N, (uint64_t)Kdim, 1, 128, 128);
         if (rc) return rc;
     } else {
@@ -638,14 +686,16 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
         const cudaError_t ce = cudaMemsetAsync(counter, 0, sizeof(int), st);
         if (ce != cudaSuccess) return cuda_fail(ce);
     }
-    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter};
-    const int NT = mode == MOE_GEMM_GATE_UP_SILU_QUANT ? N / 128 : (N + BN - 1) / BN;
+    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter, dH};
+    const int NT = gu ? N / 128 : (N + BN - 1) / BN;
     const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NT;
     const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);
-    if (gu)
-        grouped_gemm_fp8_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
+    if (kmode == 1)
+        grouped_gemm_fp8_kernel<1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
+    else if (kmode == 2)
+        grouped_gemm_fp8_kernel<2><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
     else
-        grouped_gemm_fp8_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
+        grouped_gemm_fp8_kernel<0><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
     return check_launch();
 }
 

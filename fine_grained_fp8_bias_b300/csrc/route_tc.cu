@@ -790,6 +790,71 @@ int launch_select(const uint16_t* u, const float* c, const float* bias, const fl
     return check_launch();
 }
 
+// ------------------------------------------------------------ gate term
+// Input gradient through the gates (reading R15): with dg_k = dh_t . y_k (the
+// forward's bf16 expert output of slot k), s_k = sigmoid(u_t . e_k) (exact
+// logit, as the router) and S = sum_k s_k, the gates g_k = s_k / S give
+// dl_k = (dg_k - sum_j g_j dg_j) / S * s_k (1 - s_k), and du_t += sum_k dl_k e_k.
+// One block of SEL_WARPS warps per token; the warps share the K slots.
+__global__ void __launch_bounds__(SEL_WARPS * 32) gate_term_kernel(
+    const uint16_t* __restrict__ u, const uint16_t* __restrict__ dh, const uint16_t* __restrict__ Y,
+    const int32_t* __restrict__ inv_row, const int32_t* __restrict__ idx,
+    const float* __restrict__ gate, const float* __restrict__ c, int T, int d, int K, int M,
+    float* __restrict__ du, int32_t* status) {
+    extern __shared__ __align__(16) uint16_t gt_u[];
+    __shared__ float dg_s[kMaxTopK], s_s[kMaxTopK], dl_s[kMaxTopK];
+    __shared__ int e_s[kMaxTopK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    for (int j = threadIdx.x * 8; j < d; j += SEL_WARPS * 32 * 8)
+        *reinterpret_cast<uint4*>(gt_u + j) = *reinterpret_cast<const uint4*>(u + (size_t)t * d + j);
+    __syncthreads();
+    for (int k = warp; k < K; k += SEL_WARPS) {
+        const int e = idx[(size_t)t * K + k];
+        int row = inv_row[(size_t)t * K + k];
+        if (row < 0 || row >= M) {
+            if (lane == 0) flag_status(status, MOE_ERR_BAD_INDEX);
+            row = 0;
+        }
+        float acc = 0.0f;
+        for (int j = lane * 8; j < d; j += 256) {
+            const uint4 a = *reinterpret_cast<const uint4*>(dh + (size_t)t * d + j);
+            const uint4 b = *reinterpret_cast<const uint4*>(Y + (size_t)row * d + j);
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(bf16_bits_to_float(static_cast<uint16_t>(wa[i] & 0xFFFFu)),
+                           bf16_bits_to_float(static_cast<uint16_t>(wb[i] & 0xFFFFu)), acc);
+                acc = fmaf(bf16_bits_to_float(static_cast<uint16_t>(wa[i] >> 16)),
+                           bf16_bits_to_float(static_cast<uint16_t>(wb[i] >> 16)), acc);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const float l = exact_dot(gt_u, c + (size_t)e * d, d, lane);
+        if (lane == 0) {
+            dg_s[k] = acc;
+            s_s[k] = sigmoid(l);
+            e_s[k] = e;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float S = 0.0f, gdg = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            S += s_s[k];
+            gdg = fmaf(gate[(size_t)t * K + k], dg_s[k], gdg);
+        }
+        for (int k = 0; k < K; ++k) dl_s[k] = __fdiv_rn(dg_s[k] - gdg, S) * s_s[k] * (1.0f - s_s[k]);
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < d; j += SEL_WARPS * 32) {
+        float v = 0.0f;
+        for (int k = 0; k < K; ++k) v = fmaf(dl_s[k], c[(size_t)e_s[k] * d + j], v);
+        du[(size_t)t * d + j] += v;
+    }
+}
+
 __global__ void sum_partials_kernel(const float* __restrict__ part, int split, size_t n,
                                     float* __restrict__ out) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
@@ -838,6 +903,21 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
 }  // namespace
 
 size_t route_ws_bytes(int T, int d, int E) { return route_ws(T, d, E).total; }
+
+int launch_gate_term(const uint16_t* u, const uint16_t* dh, const uint16_t* Y, const int32_t* inv_row,
+                     const int32_t* idx, const float* gate, const float* cent, int T, int d, int K,
+                     int M, float* du, int32_t* status, cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    const size_t smem = (size_t)d * 2;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(gate_term_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    gate_term_kernel<<<T, SEL_WARPS * 32, smem, st>>>(u, dh, Y, inv_row, idx, gate, cent, T, d, K, M,
+                                                      du, status);
+    return check_launch();
+}
 
 int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,
                           float* norms_out, void* ws, int32_t* status, cudaStream_t st) {

@@ -131,6 +131,35 @@ class MoELayer:
             lib.moe_forward(self.struct(), u, ws, out, side)
         return g, out
 
+    # ---------------------------------------------------------- backward
+    def prepare_backward(self, stream=None):
+        """Transposed weight blocks for the input gradient (after every change
+        of the weights)."""
+        dev, G, d, I = self.device, self.G, self.d, self.I
+        if getattr(self, "_bwd_w", None) is None:
+            self._bwd_w = (torch.empty((G, I, d), dtype=torch.uint8, device=dev),
+                           torch.empty((G, I // 128, d // 128), dtype=torch.float32, device=dev),
+                           torch.empty((G, d, 2 * I), dtype=torch.uint8, device=dev),
+                           torch.empty((G, d // 128, 2 * I // 128), dtype=torch.float32, device=dev))
+        lib.moe_prepare_backward_weights(self.struct(), *self._bwd_w, stream)
+
+    def backward_dgrad(self, u: torch.Tensor, dh: torch.Tensor, fwd: dict, stream=None) -> torch.Tensor:
+        """du of the forward that just ran on u (fwd: its outputs; the layer's
+        workspace still holds its dispatch state)."""
+        if getattr(self, "_bwd_w", None) is None:
+            self.prepare_backward(stream)
+        T = u.shape[0]
+        n = lib.moe_backward_workspace_size(self.struct(), T)
+        if getattr(self, "_bwd_ws", None) is None or self._bwd_ws.numel() < n:
+            self._bwd_ws = torch.empty(n + 256, dtype=torch.uint8, device=self.device)
+        B = lib.moe_layer_bwd_t(*(t.data_ptr() for t in self._bwd_w))
+        return lib.moe_backward_dgrad(self.struct(), B, u, dh, fwd, self.workspace(T), self._bwd_ws,
+                                      stream=stream)
+
+    def backward_status(self, stream=None) -> int:
+        ws = getattr(self, "_bwd_ws", None)
+        return lib.moe_check_device_status(ws[:16].view(torch.int32), stream) if ws is not None else 0
+
     def update_bias(self, counts: torch.Tensor, T: int, gamma: float, stream=None):
         lib.moe_update_bias(counts, self.bias, T, self.K, gamma, stream)
 

@@ -41,6 +41,10 @@ class moe_layer_t(ctypes.Structure):
                 ("n_groups", I32), ("topk_groups", I32), ("group_topk", I32)]
 
 
+class moe_layer_bwd_t(ctypes.Structure):
+    _fields_ = [("w_down_t", P), ("s_down_t", P), ("w_gu_t", P), ("s_gu_t", P)]
+
+
 class moe_batch_buffers_t(ctypes.Structure):
     _fields_ = [("u", P), ("h", P), ("topk_idx", P), ("topk_gate", P), ("tie_flag", P),
                 ("counts", P)]
@@ -60,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.moe_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
     lib.moe_route_workspace_size.restype = ctypes.c_size_t
     lib.moe_route_workspace_size.argtypes = [I32, I32, I32]
+    lib.moe_backward_workspace_size.restype = ctypes.c_size_t
+    lib.moe_backward_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
     # Every other entry point returns an int status.  Each one is called only
     # with these argument types: ctypes would otherwise pass Python ints as C
     # int and cut 64-bit pointers to 32 bits.
@@ -77,6 +83,9 @@ def _load() -> ctypes.CDLL:
         "moe_combine": [P, P, P, P, P, I32, I32, I32, I32, P, P],
         "moe_forward": [ctypes.POINTER(moe_layer_t), P, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_update_bias": [P, I32, I32, I32, ctypes.c_float, P, P],
+        "moe_prepare_backward_weights": [ctypes.POINTER(moe_layer_t), P, P, P, P, P],
+        "moe_backward_dgrad": [ctypes.POINTER(moe_layer_t), ctypes.POINTER(moe_layer_bwd_t), P, P,
+                               I32, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P],
         "moe_forward_host": [ctypes.POINTER(moe_layer_t), I32, I32, P, P, ctypes.c_float,
                              ctypes.POINTER(moe_batch_buffers_t), P, ctypes.c_size_t, P, P, P],
         "moe_check_device_status": [P, P],
@@ -383,3 +392,33 @@ def moe_forward_host(L: moe_layer_t, T: int, u_host: list, h_host: list, gamma: 
                                  ctypes.cast(h_arr, P), gamma, b_arr, _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(compute_stream),
                                  _stream(h2d_stream), _stream(d2h_stream)), "moe_forward_host")
+
+
+def moe_prepare_backward_weights(L: moe_layer_t, w_down_t: torch.Tensor, s_down_t: torch.Tensor,
+                                 w_gu_t: torch.Tensor, s_gu_t: torch.Tensor, stream=None) -> None:
+    """The transposed weight blocks the input gradient uses (exact in FP8)."""
+    _check(_lib.moe_prepare_backward_weights(ctypes.byref(L), _ptr(w_down_t), _ptr(s_down_t),
+                                             _ptr(w_gu_t), _ptr(s_gu_t), _stream(stream)),
+           "moe_prepare_backward_weights")
+
+
+def moe_backward_workspace_size(L: moe_layer_t, T: int) -> int:
+    return int(_lib.moe_backward_workspace_size(ctypes.byref(L), T))
+
+
+def moe_backward_dgrad(L: moe_layer_t, B: moe_layer_bwd_t, u: torch.Tensor, dh: torch.Tensor,
+                       fwd: dict, fwd_ws: torch.Tensor, bwd_ws: torch.Tensor,
+                       du: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """du for the forward whose outputs (idx, gate) and workspace are given."""
+    _bits(u, torch.bfloat16)
+    _bits(dh, torch.bfloat16)
+    _dev(u, "u")
+    T, d = u.shape
+    if du is None:
+        du = torch.empty((T, d), dtype=torch.float32, device=u.device)
+    _check(_lib.moe_backward_dgrad(ctypes.byref(L), ctypes.byref(B), _ptr(u), _ptr(dh), T,
+                                   _ptr(fwd["idx"]), _ptr(fwd["gate"]), _ptr(du), _ptr(fwd_ws),
+                                   fwd_ws.numel() * fwd_ws.element_size(), _ptr(bwd_ws),
+                                   bwd_ws.numel() * bwd_ws.element_size(), _stream(stream)),
+           "moe_backward_dgrad")
+    return du

@@ -56,7 +56,8 @@ enum moe_status {
 /* Grouped GEMM modes (moe_grouped_gemm_fp8). */
 enum moe_gemm_mode {
     MOE_GEMM_GATE_UP_SILU_QUANT = 1, /* h = SiLU(A W_gate^T) * (A W_up^T), re-quantised 1x128 */
-    MOE_GEMM_DOWN = 2                /* y = A W_down^T, stored as bf16                         */
+    MOE_GEMM_DOWN = 2,               /* y = A W_down^T, stored as bf16                         */
+    MOE_GEMM_GATE_UP_DGRAD = 3       /* [dG | dU] from recomputed G, U and dH (moe_backward_dgrad) */
 };
 
 /* One DeepSeekMoE layer: d hidden, E routed experts (top-K of them per
@@ -292,6 +293,48 @@ typedef struct moe_batch_buffers_t {
 int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t* const* u_host,
                      float* const* h_host, float gamma, const moe_batch_buffers_t* buf, void* ws,
                      size_t ws_bytes, void* compute_stream, void* h2d_stream, void* d2h_stream);
+
+/* Input gradient of the layer (the pages: FP8 also carries part of the
+ * gradient propagation, [SYH] FP8 資料格式訓練; they wish for transposed
+ * GEMMs in hardware, [YLY] hardware suggestions).  Reading: every expert
+ * backward GEMM follows the forward's FP8 rule.  The transposed weights are
+ * exact in FP8 with 128x128 block scales (codes moved, each block keeps its
+ * scale); moe_prepare_backward_weights writes them once per weight update:
+ *   w_down_t [E+S, I, d] fp8 with s_down_t [E+S, I/128, d/128],
+ *   w_gu_t   [E+S, d, 2I] fp8 = [W_gate^T | W_up^T] with s_gu_t [E+S, d/128, 2I/128]. */
+typedef struct moe_layer_bwd_t {
+    const uint8_t* w_down_t;
+    const float* s_down_t;
+    const uint8_t* w_gu_t;
+    const float* s_gu_t;
+} moe_layer_bwd_t;
+
+int moe_prepare_backward_weights(const moe_layer_t* L, uint8_t* w_down_t, float* s_down_t,
+                                 uint8_t* w_gu_t, float* s_gu_t, void* stream);
+
+/* Workspace bytes moe_backward_dgrad needs for up to T_max tokens (0 if L is
+ * invalid); its first 16 bytes hold the call's device status word. */
+size_t moe_backward_workspace_size(const moe_layer_t* L, int T_max);
+
+/* du = d loss / d u for a forward that has just run: call after moe_forward
+ * with the same L, u and T, and pass that call's workspace (fwd_ws; its
+ * dispatched activations, group offsets, dispatch rows and expert outputs
+ * are read) and routing (topk_idx, topk_gate).  dh [T, d] bf16 is the
+ * gradient of h'; du [T, d] float32.  Steps: the gradient of each dispatch
+ * row (g_k dh routed, dh shared; float32 product) quantised per 1x128 tile;
+ * dH = bf16(dy W_down); G and U recomputed by the gate/up GEMM, whose
+ * epilogue forms dG = dH U sigma (1 + G (1 - sigma)), dU = dH G sigma
+ * (sigma = 1 / (1 + e^-G)) and quantises [dG | dU] per 1x128 tile;
+ * dA = bf16([dG | dU] [W_gate ; W_up]); du = dh + the token's rows of dA, plus
+ * the gates' dependence on u: with dg_k = dh . y_k, s_k = sigmoid(u . e_k)
+ * (exact logit, as moe_route) and S = sum s_k,
+ * du += sum_k (dg_k - sum_j g_j dg_j) / S * s_k (1 - s_k) e_k.  The bias has no
+ * gradient.  bwd_ws: moe_backward_workspace_size(L, T) bytes, 256-byte
+ * aligned; moe_check_device_status(bwd_ws, stream) reads its status. */
+int moe_backward_dgrad(const moe_layer_t* L, const moe_layer_bwd_t* B, const uint16_t* u,
+                       const uint16_t* dh, int T, const int32_t* topk_idx, const float* topk_gate,
+                       float* du, void* fwd_ws, size_t fwd_ws_bytes, void* bwd_ws,
+                       size_t bwd_ws_bytes, void* stream);
 
 /* Auxiliary-loss-free bias update at the end of a step ([TH] Method §2:
  * b_i -= gamma when expert i is overloaded, += gamma when underloaded;
