@@ -332,6 +332,7 @@ def run_ours(args, world, rank, local):
     e2e = run_e2e(layer, cfg, dev, max(3, min(args.steps, 50)), world)
     decode = run_decode(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
     balance = run_balance(layer, cfg, dev) if args.workload == "v3_long" else None
+    backward = run_backward(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -347,6 +348,8 @@ def run_ours(args, world, rank, local):
         line["decode"] = decode
     if balance:
         line["balance"] = balance
+    if backward:
+        line["backward_dgrad"] = backward
     return line
 
 
@@ -416,6 +419,38 @@ def run_decode(layer, cfg, dev, pk, Ts=(1, 16, 64, 256), steps=50):
         layer.centroids.copy_(saved_c)
         layer.bias.copy_(saved_b)
     return res
+
+
+def run_backward(layer, cfg, dev, pk, steps=20):
+    """Input gradient of the layer (moe_backward_dgrad) after a forward of the
+    same batch: time of the backward alone (CUDA events), its GEMM FLOP rate
+    (10 M d I: dH, the recomputed gate/up, dA) and the rate of the weight bytes
+    it reads (W_down^T, W_gate, W_up, [W_gate^T | W_up^T] of the touched groups)."""
+    u = wl.tokens(cfg, dev)
+    dh = wl.normal(wl.stream_key(cfg.seed, 99), (cfg.T, cfg.d), 1.0, dev).to(torch.bfloat16)
+    out = layer.forward(u)
+    layer.prepare_backward()
+    for _ in range(3):
+        layer.backward_dgrad(u, dh, out)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        layer.backward_dgrad(u, dh, out)
+    e.record()
+    torch.cuda.synchronize()
+    if layer.backward_status() != 0:
+        raise RuntimeError("device status flagged in the backward leg")
+    ms = s.elapsed_time(e) / steps
+    M = cfg.T * (cfg.K + cfg.S)
+    flops = 10.0 * M * cfg.d * cfg.I
+    touched = int((out["counts"].cpu() > 0).sum()) + cfg.S
+    wbytes = touched * 5 * cfg.d * cfg.I
+    return {"ms": round(ms, 4), "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1),
+            "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "what": "du from dh' (bf16) for the V3 batch: quantise dy, dH GEMM, gate/up recompute "
+                    "+ SiLU backward + re-quantise, dA GEMM, gather, gate term"}
 
 
 def run_balance(layer, cfg, dev, steps=100):
