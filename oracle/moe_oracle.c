@@ -50,6 +50,10 @@
  *       b_e -= gamma or += gamma in float32; equal load leaves b_e unchanged.
  *   R15 input gradient of the layer: the backward GEMMs follow the
  *       forward's FP8 rule (see orc_layer_backward_dgrad).
+ *   R16 weight gradients: the FP8 tensors the layer holds are dequantised,
+ *       transposed and re-quantised in 128x1 tiles along each expert's
+ *       dispatch rows; both operands of the token-contracted GEMM carry a
+ *       scale per row per slab (see orc_layer_backward_wgrad).
  *   R14 group-limited routing (the pages: a token goes to at most M = 4
  *       nodes, no scoring rule given): experts form n_groups contiguous
  *       groups; group score = float32 sum, largest first, of the group's
@@ -628,6 +632,169 @@ void orc_layer_backward_dgrad(const uint16_t* u, int T, int d, int E, int K, int
     free(qa); free(sa); free(G); free(U); free(h); free(qh); free(sh); free(y); free(dy);
     free(qdy); free(sdy); free(dH); free(dgu); free(qgu); free(sgu); free(dA); free(dhf);
     free(acc); free(dg); free(wdT); free(sdT); free(wguT); free(sguT); free(tq); free(ts);
+}
+
+/* ------------------------------------------------------------------ */
+/* Weight gradients of one expert (R16).  The pages keep master weights  */
+/* and their gradients in 16/32 bits and FP8 activations in storage      */
+/* ("DeepSeek V3技術報告", FP8 資料格式訓練; "官方揭秘DeepSeek-V3模型训练 */
+/* 全流程" §4.3 low-precision storage), and ask for transposed GEMMs in   */
+/* hardware (same page, hardware suggestions) because the FP8 tensors     */
+/* the forward holds in 1x128 tiles along features must be contracted     */
+/* over tokens here.  Reading: the four FP8 tensors the layer already     */
+/* holds -- the activation rows A and h of the forward, dy and [dG | dU]  */
+/* of the input gradient (R15) -- are each dequantised (x = dec(q) s, a   */
+/* float32 product), transposed and re-quantised in 128x1 tiles: 128      */
+/* consecutive dispatch rows of one expert (the expert's last block       */
+/* ragged; a block never spans two experts) by one column, with R2's      */
+/* rule.  Then dW_down = dy^T h and [dW_gate ; dW_up] = [dG | dU]^T A,    */
+/* each entry summed over 128-row slabs with R7's promotion, where both   */
+/* operands carry one scale per row per slab:                            */
+/*   acc = fmaf(p, sA * sB, acc),  sA * sB a float32 product.             */
+/* Output float32.  An expert that no token selected gets dW = 0.         */
+/* ------------------------------------------------------------------ */
+
+/* q [M, C] codes with 1x128 scales s [M, C/128] -> the 128x1 form:
+ * qt [C, Mp] codes (Mp = M rounded up to 128; codes past row M are 0) and
+ * st [C, Mp/128] scales. */
+void orc_requant_128x1(const uint8_t* q, const float* s, int M, int C, uint8_t* qt, float* st) {
+    const int nb = (M + 127) / 128, Mp = nb * 128;
+    float* col = (float*)malloc(sizeof(float) * 128);
+    init_dec();
+    for (int c = 0; c < C; ++c)
+        for (int b = 0; b < nb; ++b) {
+            const int r0 = b * 128, n = M - r0 < 128 ? M - r0 : 128;
+            for (int i = 0; i < n; ++i) {
+                const float v = (float)g_dec[q[(int64_t)(r0 + i) * C + c]];
+                col[i] = v * s[(int64_t)(r0 + i) * (C / 128) + c / 128];
+            }
+            uint8_t* dst = qt + (int64_t)c * Mp + r0;
+            st[(int64_t)c * nb + b] = quant_tile(col, n, 1, dst, 1);
+            for (int i = n; i < 128; ++i) dst[i] = 0x00;
+        }
+    free(col);
+}
+
+/* out[n, m] = sum over K slabs of (exact slab dot product) * sa * sb with
+ * one scale per row per slab on both sides, accumulated in float32 (R16).
+ *   qa [Na, Kd], sa [Na, Kd/128];  qb [Nb, Kd], sb [Nb, Kd/128];  out [Na, Nb]. */
+void orc_gemm_fp8_rowscaled(const uint8_t* qa, const float* sa, int Na, int Kd,
+                            const uint8_t* qb, const float* sb, int Nb, float* out) {
+    int kb_n = Kd / 128;
+    init_dec();
+    for (int n = 0; n < Na; ++n)
+        for (int m = 0; m < Nb; ++m) {
+            float acc = 0.0f;
+            for (int kb = 0; kb < kb_n; ++kb) {
+                double p = 0.0;
+                for (int k = kb * 128; k < kb * 128 + 128; ++k)
+                    p += g_dec[qa[(int64_t)n * Kd + k]] * g_dec[qb[(int64_t)m * Kd + k]];
+                float sc = sa[(int64_t)n * kb_n + kb] * sb[(int64_t)m * kb_n + kb];
+                acc = fmaf((float)p, sc, acc);
+            }
+            out[(int64_t)n * Nb + m] = acc;
+        }
+}
+
+/* dW_gate, dW_up [I, d] and dW_down [d, I] (float32) of group g: routed
+ * expert g < E takes the tokens that selected it, in ascending order (R6),
+ * with their gates; shared expert g >= E takes every token with weight 1.
+ * wg, wu [I, d] and wd [d, I] are that group's weights with their block
+ * scales; u, dh [T, d] bf16; idx, gate [T, K] the forward's routing. */
+void orc_layer_backward_wgrad(const uint16_t* u, int T, int d, int E, int K, int I,
+                              const int32_t* idx, const float* gate, const uint8_t* wg,
+                              const float* sg, const uint8_t* wu, const float* su,
+                              const uint8_t* wd, const float* sd, const uint16_t* dh, int g,
+                              float* dWg, float* dWu, float* dWd) {
+    /* the group's dispatch rows */
+    int* tok = (int*)malloc(sizeof(int) * (size_t)(T > 0 ? T : 1));
+    float* gk = (float*)malloc(sizeof(float) * (size_t)(T > 0 ? T : 1));
+    int m = 0;
+    for (int t = 0; t < T; ++t) {
+        if (g >= E) {
+            tok[m] = t; gk[m] = 1.0f; ++m;
+            continue;
+        }
+        for (int k = 0; k < K; ++k)
+            if (idx[(int64_t)t * K + k] == g) {
+                tok[m] = t; gk[m] = gate[(int64_t)t * K + k]; ++m;
+                break;
+            }
+    }
+    if (m == 0) {
+        memset(dWg, 0, sizeof(float) * (size_t)I * d);
+        memset(dWu, 0, sizeof(float) * (size_t)I * d);
+        memset(dWd, 0, sizeof(float) * (size_t)d * I);
+        free(tok); free(gk);
+        return;
+    }
+    const int nb = (m + 127) / 128, Mp = nb * 128;
+    uint8_t* qa = (uint8_t*)malloc((size_t)m * d);
+    float* sa = (float*)malloc(sizeof(float) * (size_t)m * (d / 128));
+    float* G = (float*)malloc(sizeof(float) * (size_t)m * I);
+    float* U = (float*)malloc(sizeof(float) * (size_t)m * I);
+    float* h = (float*)malloc(sizeof(float) * (size_t)m * I);
+    uint8_t* qh = (uint8_t*)malloc((size_t)m * I);
+    float* sh = (float*)malloc(sizeof(float) * (size_t)m * (I / 128));
+    float* dy = (float*)malloc(sizeof(float) * (size_t)m * d);
+    uint8_t* qdy = (uint8_t*)malloc((size_t)m * d);
+    float* sdy = (float*)malloc(sizeof(float) * (size_t)m * (d / 128));
+    uint8_t* wdT = (uint8_t*)malloc((size_t)I * d);
+    float* sdT = (float*)malloc(sizeof(float) * (size_t)(I / 128) * (d / 128));
+    float* dH = (float*)malloc(sizeof(float) * (size_t)m * I);
+    float* dgu = (float*)malloc(sizeof(float) * (size_t)m * 2 * I);
+    uint8_t* qgu = (uint8_t*)malloc((size_t)m * 2 * I);
+    float* sgu = (float*)malloc(sizeof(float) * (size_t)m * (2 * I / 128));
+    uint8_t* at = (uint8_t*)malloc((size_t)d * Mp);
+    float* sat = (float*)malloc(sizeof(float) * (size_t)d * nb);
+    uint8_t* ht = (uint8_t*)malloc((size_t)I * Mp);
+    float* sht = (float*)malloc(sizeof(float) * (size_t)I * nb);
+    uint8_t* dyt = (uint8_t*)malloc((size_t)d * Mp);
+    float* sdyt = (float*)malloc(sizeof(float) * (size_t)d * nb);
+    uint8_t* gut = (uint8_t*)malloc((size_t)2 * I * Mp);
+    float* sgut = (float*)malloc(sizeof(float) * (size_t)2 * I * nb);
+    float* dWgu = (float*)malloc(sizeof(float) * (size_t)2 * I * d);
+
+    /* the forward's FP8 activation rows and h */
+    for (int r = 0; r < m; ++r)
+        orc_quant_1x128_bf16(u + (int64_t)tok[r] * d, 1, d, qa + (int64_t)r * d, sa + (int64_t)r * (d / 128));
+    orc_gemm_fp8(qa, sa, m, d, wg, sg, I, G);
+    orc_gemm_fp8(qa, sa, m, d, wu, su, I, U);
+    for (int64_t i = 0; i < (int64_t)m * I; ++i) h[i] = G[i] / (1.0f + expf(-G[i])) * U[i];
+    orc_quant_1x128_f32(h, m, I, qh, sh);
+    /* the input gradient's FP8 dy and [dG | dU] (R15) */
+    for (int r = 0; r < m; ++r)
+        for (int j = 0; j < d; ++j) {
+            const float v = bf16_to_f32(dh[(int64_t)tok[r] * d + j]);
+            dy[(int64_t)r * d + j] = g >= E ? v : gk[r] * v;
+        }
+    orc_quant_1x128_f32(dy, m, d, qdy, sdy);
+    transpose_blocks(wd, sd, d, I, wdT, sdT);
+    orc_gemm_fp8(qdy, sdy, m, d, wdT, sdT, I, dH);
+    for (int r = 0; r < m; ++r)
+        for (int i = 0; i < I; ++i) {
+            const int64_t x = (int64_t)r * I + i;
+            const float dHv = bf16_round(dH[x]);
+            const float sgm = 1.0f / (1.0f + expf(-G[x]));
+            dgu[(int64_t)r * 2 * I + i] = dHv * U[x] * sgm * (1.0f + G[x] * (1.0f - sgm));
+            dgu[(int64_t)r * 2 * I + I + i] = dHv * G[x] * sgm;
+        }
+    orc_quant_1x128_f32(dgu, m, 2 * I, qgu, sgu);
+    /* dequantise, transpose, re-quantise in 128x1 tiles */
+    orc_requant_128x1(qa, sa, m, d, at, sat);
+    orc_requant_128x1(qh, sh, m, I, ht, sht);
+    orc_requant_128x1(qdy, sdy, m, d, dyt, sdyt);
+    orc_requant_128x1(qgu, sgu, m, 2 * I, gut, sgut);
+    /* dW_down = dy^T h;  [dW_gate ; dW_up] = [dG | dU]^T A */
+    orc_gemm_fp8_rowscaled(dyt, sdyt, d, Mp, ht, sht, I, dWd);
+    orc_gemm_fp8_rowscaled(gut, sgut, 2 * I, Mp, at, sat, d, dWgu);
+    memcpy(dWg, dWgu, sizeof(float) * (size_t)I * d);
+    memcpy(dWu, dWgu + (int64_t)I * d, sizeof(float) * (size_t)I * d);
+
+    free(tok); free(gk); free(qa); free(sa); free(G); free(U); free(h); free(qh); free(sh);
+    free(dy); free(qdy); free(sdy); free(wdT); free(sdT); free(dH); free(dgu); free(qgu);
+    free(sgu); free(at); free(sat); free(ht); free(sht); free(dyt); free(sdyt); free(gut);
+    free(sgut); free(dWgu);
 }
 
 /* ------------------------------------------------------------------ */

@@ -61,6 +61,10 @@ def lib() -> ctypes.CDLL:
         _lib.orc_update_bias.argtypes = [P, i32, i32, i32, ctypes.c_float, P]
         _lib.orc_layer_backward_dgrad.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P,
                                                   P, P, P, P, P, P, P, P, i32, P]
+        _lib.orc_requant_128x1.argtypes = [P, P, i32, i32, P, P]
+        _lib.orc_gemm_fp8_rowscaled.argtypes = [P, P, i32, i32, P, P, i32, P]
+        _lib.orc_layer_backward_wgrad.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P,
+                                                  P, P, P, i32, P, P, P]
     return _lib
 
 
@@ -268,6 +272,49 @@ def layer_backward_dgrad(u_bits, idx, gate, W: Weights, cent, dh_bits, d: int, E
                                    ptrs(W.down, 0), ptrs(W.down, 1), _p(dh_bits), _p(tok),
                                    len(tok), _p(out))
     return out
+
+
+def requant_128x1(q, s) -> tuple[np.ndarray, np.ndarray]:
+    """Reading R16: codes q [M, C] with 1x128 scales s [M, C/128] ->
+    (codes [C, Mp], scales [C, Mp/128]) in 128x1 tiles, Mp = M rounded up to 128."""
+    q, s = _c(q, np.uint8), _c(s, np.float32)
+    M, C = q.shape
+    nb = (M + 127) // 128
+    qt = np.empty((C, nb * 128), np.uint8)
+    st = np.empty((C, nb), np.float32)
+    lib().orc_requant_128x1(_p(q), _p(s), M, C, _p(qt), _p(st))
+    return qt, st
+
+
+def gemm_fp8_rowscaled(qa, sa, qb, sb) -> np.ndarray:
+    """Token-contracted FP8 GEMM of reading R16: qa [Na, K], sa [Na, K/128];
+    qb [Nb, K], sb [Nb, K/128] -> float32 [Na, Nb]."""
+    qa, sa, qb, sb = _c(qa, np.uint8), _c(sa, np.float32), _c(qb, np.uint8), _c(sb, np.float32)
+    Na, K = qa.shape
+    Nb = qb.shape[0]
+    assert qb.shape[1] == K and sa.shape == (Na, K // 128) and sb.shape == (Nb, K // 128)
+    out = np.empty((Na, Nb), np.float32)
+    lib().orc_gemm_fp8_rowscaled(_p(qa), _p(sa), Na, K, _p(qb), _p(sb), Nb, _p(out))
+    return out
+
+
+def layer_backward_wgrad(u_bits, idx, gate, w_group, dh_bits, d: int, E: int, K: int, I: int,
+                         g: int) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Reading R16: (dW_gate [I, d], dW_up [I, d], dW_down [d, I]) float32 of
+    group g.  w_group = ((wg, sg), (wu, su), (wd, sd)) of that group."""
+    u_bits, dh_bits = _c(u_bits, np.uint16), _c(dh_bits, np.uint16)
+    idx, gate = _c(idx, np.int32), _c(gate, np.float32)
+    (wg, sg), (wu, su), (wd, sd) = w_group
+    wg, wu, wd = _c(wg, np.uint8), _c(wu, np.uint8), _c(wd, np.uint8)
+    sg, su, sd = _c(sg, np.float32), _c(su, np.float32), _c(sd, np.float32)
+    T = u_bits.shape[0]
+    dWg = np.empty((I, d), np.float32)
+    dWu = np.empty((I, d), np.float32)
+    dWd = np.empty((d, I), np.float32)
+    lib().orc_layer_backward_wgrad(_p(u_bits), T, d, E, K, I, _p(idx), _p(gate), _p(wg), _p(sg),
+                                   _p(wu), _p(su), _p(wd), _p(sd), _p(dh_bits), g, _p(dWg),
+                                   _p(dWu), _p(dWd))
+    return dWg, dWu, dWd
 
 
 def update_bias(counts, bias, T: int, K: int, gamma: float) -> np.ndarray:
