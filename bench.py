@@ -333,6 +333,7 @@ def run_ours(args, world, rank, local):
     decode = run_decode(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
     balance = run_balance(layer, cfg, dev) if args.workload == "v3_long" else None
     backward = run_backward(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
+    wgrad = run_wgrad(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -350,6 +351,8 @@ def run_ours(args, world, rank, local):
         line["balance"] = balance
     if backward:
         line["backward_dgrad"] = backward
+    if wgrad is not None:
+        line["backward_wgrad"] = wgrad
     return line
 
 
@@ -451,6 +454,40 @@ def run_backward(layer, cfg, dev, pk, steps=20):
             "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "what": "du from dh' (bf16) for the V3 batch: quantise dy, dH GEMM, gate/up recompute "
                     "+ SiLU backward + re-quantise, dA GEMM, gather, gate term"}
+
+
+def run_wgrad(layer, cfg, dev, pk, steps=10):
+    """Weight gradients of every expert (moe_backward_wgrad) for the batch of
+    the backward leg: time of the call alone (CUDA events; four 128x1
+    re-quantisations and two token-contracted GEMMs), the float32 gradient
+    bytes it writes (3 d I per group) as a rate, and its GEMM FLOP rate
+    (6 M d I over the dispatch rows)."""
+    T = cfg.T
+    dW = layer.backward_wgrad(T)
+    for _ in range(2):
+        layer.backward_wgrad(T, dW)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        layer.backward_wgrad(T, dW)
+    e.record()
+    torch.cuda.synchronize()
+    if layer.backward_status() != 0:
+        raise RuntimeError("device status flagged in the weight-gradient leg")
+    ms = s.elapsed_time(e) / steps
+    G = cfg.E + cfg.S
+    out_bytes = G * 3 * cfg.d * cfg.I * 4
+    M = T * (cfg.K + cfg.S)
+    flops = 6.0 * M * cfg.d * cfg.I
+    del dW
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "out_GB": round(out_bytes / 1e9, 2),
+            "out_GBps": round(out_bytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(out_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1),
+            "what": "dW_gate, dW_up, dW_down (float32) of all 257 experts for the V3 batch: "
+                    "A, h, dy, [dG | dU] re-quantised 128x1, then dy^T h and [dG | dU]^T A"}
 
 
 def run_balance(layer, cfg, dev, steps=100):

@@ -350,6 +350,40 @@ BwdLayout bwd_layout(int T, int d, int K, int S, int I) {
     return L;
 }
 
+// The re-quantised operands of the weight gradient (128x1 tiles, padded
+// layout of moe_requant_128x1): ld columns each, scales [ld/128, C].
+struct WgLayout {
+    long long ld;
+    size_t at, sat, ht, sht, dyt, sdyt, gut, sgut, total;
+};
+
+WgLayout wg_layout(int T, int d, int G, int K, int S, int I) {
+    WgLayout L{};
+    const long long M = (long long)T * (K + S);
+    L.ld = (M + 127LL * G + 127) / 128 * 128;
+    if (L.ld > 0x7fffffffLL) {
+        L.ld = -1;
+        return L;
+    }
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    const size_t ld = (size_t)L.ld, nsl = ld / 128;
+    L.at = take(ld * d);
+    L.sat = take(sizeof(float) * nsl * d);
+    L.ht = take(ld * I);
+    L.sht = take(sizeof(float) * nsl * I);
+    L.dyt = take(ld * d);
+    L.sdyt = take(sizeof(float) * nsl * d);
+    L.gut = take(ld * 2 * I);
+    L.sgut = take(sizeof(float) * nsl * 2 * I);
+    L.total = off;
+    return L;
+}
+
 struct EventSet {
     cudaEvent_t ev[6] = {};
     ~EventSet() {
@@ -451,6 +485,111 @@ int moe_backward_dgrad(const moe_layer_t* L, const moe_layer_bwd_t* B, const uin
         return rc;
     return launch_gate_term(u, dh, Y, inv_row, topk_idx, topk_gate, L->centroids, T, d, K, M, du,
                             status, st);
+}
+
+int moe_wgrad_ld(int M, int G) {
+    if (M < 0 || G < 0) return 0;
+    const long long ld = ((long long)M + 127LL * G + 127) / 128 * 128;
+    return ld > 0x7fffffffLL ? 0 : (int)ld;
+}
+
+int moe_requant_128x1(const uint8_t* q, const float* scales, int M, int C,
+                      const int32_t* group_offsets, int G, uint8_t* qt, float* st, int ld,
+                      int32_t* status, void* stream) {
+    if (M < 0 || C <= 0 || G < 0 || ld < 0) return MOE_ERR_INVALID_ARG;
+    if (C % 128 || G > kMaxGroups || ld % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || G == 0) return MOE_OK;
+    if (!q || !scales || !group_offsets || !qt || !st) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(qt)) return MOE_ERR_MISALIGNED;
+    if ((long long)M * C > (1LL << 40) || (long long)ld * C > (1LL << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return launch_requant_128x1(q, scales, M, C, group_offsets, G, qt, st, ld, status, S_(stream));
+}
+
+int moe_wgrad_gemm_fp8(const uint8_t* At, const float* sAt, int Na, const uint8_t* Bt,
+                       const float* sBt, int Nb, int ld, const int32_t* group_offsets, int G,
+                       float* out0, float* out1, int split, int32_t* status, void* stream) {
+    if (Na <= 0 || Nb <= 0 || G < 0 || ld < 0 || split <= 0 || split > Na) return MOE_ERR_INVALID_ARG;
+    if (Na % 128 || Nb % 128 || split % 128 || ld % 16 || G > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)G * Na > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (G == 0) return MOE_OK;
+    if (!At || !sAt || !Bt || !sBt || !group_offsets || !out0 || (split < Na && !out1))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(At) || !aligned16(Bt) || !aligned16(out0) || !aligned16(out1) ||
+        !aligned16(sAt) || !aligned16(sBt))
+        return MOE_ERR_MISALIGNED;
+    return launch_wgrad_gemm(At, sAt, Na, Bt, sBt, Nb, ld, group_offsets, G, out0, out1, split,
+                             status, S_(stream));
+}
+
+size_t moe_wgrad_workspace_size(const moe_layer_t* L, int T_max) {
+    if (check_layer(L) || T_max < 0) return 0;
+    const WgLayout W = wg_layout(T_max, L->d, L->E + L->S, L->K, L->S, L->I);
+    return W.ld < 0 ? 0 : W.total;
+}
+
+int moe_backward_wgrad(const moe_layer_t* L, int T, float* dW_gate, float* dW_up, float* dW_down,
+                       void* fwd_ws, size_t fwd_ws_bytes, void* bwd_ws, size_t bwd_ws_bytes,
+                       void* wgrad_ws, size_t wgrad_ws_bytes, void* stream) {
+    int rc = check_layer(L);
+    if (rc) return rc;
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (!dW_gate || !dW_up || !dW_down || !fwd_ws || !bwd_ws || !wgrad_ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dW_gate) || !aligned16(dW_up) || !aligned16(dW_down)) return MOE_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(fwd_ws) | reinterpret_cast<uintptr_t>(bwd_ws) |
+         reinterpret_cast<uintptr_t>(wgrad_ws)) & 255u)
+        return MOE_ERR_MISALIGNED;
+    if ((long long)T * (L->K + L->S) > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int d = L->d, E = L->E, K = L->K, S = L->S, I = L->I, G = E + S;
+    const Layout W = layout(T, d, E, K, S, I);
+    const BwdLayout BW = bwd_layout(T, d, K, S, I);
+    const WgLayout WG = wg_layout(T, d, G, K, S, I);
+    if (WG.ld < 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (fwd_ws_bytes < W.total || bwd_ws_bytes < BW.total || wgrad_ws_bytes < WG.total)
+        return MOE_ERR_WORKSPACE;
+    const cudaStream_t st = S_(stream);
+    if (T == 0) {                                    // no rows: every gradient is zero
+        const size_t n = (size_t)G * I * d * sizeof(float);
+        cudaError_t e = cudaMemsetAsync(dW_gate, 0, n, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW_up, 0, n, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW_down, 0, n, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+    }
+    char* fb = static_cast<char*>(fwd_ws);
+    char* bb = static_cast<char*>(bwd_ws);
+    char* wb = static_cast<char*>(wgrad_ws);
+    int32_t* status = reinterpret_cast<int32_t*>(bb + BW.status);
+    const int32_t* go = reinterpret_cast<const int32_t*>(fb + W.go);
+    const int M = T * (K + S), ld = WG.ld;
+    uint8_t* at = reinterpret_cast<uint8_t*>(wb + WG.at);
+    uint8_t* ht = reinterpret_cast<uint8_t*>(wb + WG.ht);
+    uint8_t* dyt = reinterpret_cast<uint8_t*>(wb + WG.dyt);
+    uint8_t* gut = reinterpret_cast<uint8_t*>(wb + WG.gut);
+    float* sat = reinterpret_cast<float*>(wb + WG.sat);
+    float* sht = reinterpret_cast<float*>(wb + WG.sht);
+    float* sdyt = reinterpret_cast<float*>(wb + WG.sdyt);
+    float* sgut = reinterpret_cast<float*>(wb + WG.sgut);
+    // the four held FP8 tensors in 128x1 tiles
+    if ((rc = launch_requant_128x1(reinterpret_cast<const uint8_t*>(fb + W.A),
+                                   reinterpret_cast<const float*>(fb + W.sa), M, d, go, G, at, sat, ld,
+                                   status, st)))
+        return rc;
+    if ((rc = launch_requant_128x1(reinterpret_cast<const uint8_t*>(fb + W.H),
+                                   reinterpret_cast<const float*>(fb + W.sh), M, I, go, G, ht, sht, ld,
+                                   status, st)))
+        return rc;
+    if ((rc = launch_requant_128x1(reinterpret_cast<const uint8_t*>(bb + BW.dyq),
+                                   reinterpret_cast<const float*>(bb + BW.sdy), M, d, go, G, dyt, sdyt,
+                                   ld, status, st)))
+        return rc;
+    if ((rc = launch_requant_128x1(reinterpret_cast<const uint8_t*>(bb + BW.dgu),
+                                   reinterpret_cast<const float*>(bb + BW.sgu), M, 2 * I, go, G, gut,
+                                   sgut, ld, status, st)))
+        return rc;
+    // dW_down = dy^T h
+    if ((rc = launch_wgrad_gemm(dyt, sdyt, d, ht, sht, I, ld, go, G, dW_down, nullptr, d, status, st)))
+        return rc;
+    // [dW_gate ; dW_up] = [dG | dU]^T A
+    return launch_wgrad_gemm(gut, sgut, 2 * I, at, sat, d, ld, go, G, dW_gate, dW_up, I, status, st);
 }
 
 int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t* const* u_host,

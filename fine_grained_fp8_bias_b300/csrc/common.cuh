@@ -77,6 +77,12 @@ int launch_quant_dy(const uint16_t* dh, int T, int d, const float* gate, const i
 int launch_gate_term(const uint16_t* u, const uint16_t* dh, const uint16_t* Y, const int32_t* inv_row,
                      const int32_t* idx, const float* gate, const float* cent, int T, int d, int K,
                      int M, float* du, int32_t* status, cudaStream_t st);
+// Weight gradients (wgrad.cu).
+int launch_requant_128x1(const uint8_t* q, const float* s, int M, int C, const int32_t* go, int G,
+                         uint8_t* qt, float* st, int ld, int32_t* status, cudaStream_t stream);
+int launch_wgrad_gemm(const uint8_t* At, const float* sAt, int Na, const uint8_t* Bt,
+                      const float* sBt, int Nb, int ld, const int32_t* go, int G, float* out0,
+                      float* out1, int split, int32_t* status, cudaStream_t st);
 int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);

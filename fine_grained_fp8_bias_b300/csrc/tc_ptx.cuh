@@ -192,6 +192,64 @@ __device__ __forceinline__ void fma2_scale(float* acc, const uint32_t* v, float 
     }
 }
 
+// acc[i] = fma(v[i], sa * sb[i], acc[i]) for N columns, sa * sb[i] a float32
+// product (packed two-lane multiply and FMA, the same bits as mulf / fmaf);
+// sb points to 16-byte aligned shared memory.
+template <int N>
+__device__ __forceinline__ void fma2_rowcol(float* acc, const uint32_t* v, float sa, const float* sb) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+        const float4 s4 = *reinterpret_cast<const float4*>(sb + i);
+        asm("{\n\t.reg .b64 d, a, s, t;\n\t"
+            "mov.b64 d, {%0, %1};\n\t"
+            "mov.b64 a, {%2, %3};\n\t"
+            "mov.b64 s, {%4, %5};\n\t"
+            "mov.b64 t, {%6, %6};\n\t"
+            "mul.rn.f32x2 s, s, t;\n\t"
+            "fma.rn.f32x2 d, a, s, d;\n\t"
+            "mov.b64 {%0, %1}, d;\n\t}"
+            : "+f"(acc[i]), "+f"(acc[i + 1])
+            : "r"(v[i]), "r"(v[i + 1]), "f"(s4.x), "f"(s4.y), "f"(sa));
+        asm("{\n\t.reg .b64 d, a, s, t;\n\t"
+            "mov.b64 d, {%0, %1};\n\t"
+            "mov.b64 a, {%2, %3};\n\t"
+            "mov.b64 s, {%4, %5};\n\t"
+            "mov.b64 t, {%6, %6};\n\t"
+            "mul.rn.f32x2 s, s, t;\n\t"
+            "fma.rn.f32x2 d, a, s, d;\n\t"
+            "mov.b64 {%0, %1}, d;\n\t}"
+            : "+f"(acc[i + 2]), "+f"(acc[i + 3])
+            : "r"(v[i + 2]), "r"(v[i + 3]), "f"(s4.z), "f"(s4.w), "f"(sa));
+    }
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+                 : "memory");
+}
+
+// TMA tile store shared -> global (bulk-group completion), and its waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one store group still reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// every store group complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy writes to shared memory become visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Wait for this thread's outstanding TMEM loads.  The registers pass through
 // the asm as read-write operands, so no use of them can move above the wait.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
@@ -204,8 +262,9 @@ __device__ __forceinline__ void reg_after_wait(uint32_t (&r)[32]) {
 
 
 // ------------------------------------------------------------ host side
-// 2-D tensor [rows, cols] of `elem_bytes`-byte elements (cols contiguous),
-// box [box_rows, box_cols], 128-byte swizzle (box_cols * elem_bytes == 128).
+// 2-D tensor [rows, cols] of `elem_bytes`-byte elements (cols contiguous;
+// 1 = E4M3 codes, 2 = bf16, 4 = float32), box [box_rows, box_cols], 128-byte
+// swizzle (box_cols * elem_bytes == 128).
 int make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, int elem_bytes,
                 uint32_t box_rows, uint32_t box_cols);
 

@@ -156,6 +156,24 @@ class MoELayer:
         return lib.moe_backward_dgrad(self.struct(), B, u, dh, fwd, self.workspace(T), self._bwd_ws,
                                       stream=stream)
 
+    def backward_wgrad(self, T: int, out: tuple | None = None, stream=None) -> tuple:
+        """Weight gradients (dW_gate [G, I, d], dW_up [G, I, d], dW_down [G, d, I],
+        float32) of the batch of T tokens whose forward and backward_dgrad just
+        ran; out: optional preallocated triple."""
+        if getattr(self, "_bwd_ws", None) is None:
+            raise RuntimeError("backward_wgrad needs the workspace of backward_dgrad")
+        n = lib.moe_wgrad_workspace_size(self.struct(), T)
+        if getattr(self, "_wg_ws", None) is None or self._wg_ws.numel() < n:
+            self._wg_ws = torch.empty(n + 256, dtype=torch.uint8, device=self.device)
+        G, d, I = self.G, self.d, self.I
+        if out is None:
+            out = (torch.empty((G, I, d), dtype=torch.float32, device=self.device),
+                   torch.empty((G, I, d), dtype=torch.float32, device=self.device),
+                   torch.empty((G, d, I), dtype=torch.float32, device=self.device))
+        lib.moe_backward_wgrad(self.struct(), T, self.workspace(T), self._bwd_ws, self._wg_ws, *out,
+                               stream=stream)
+        return out
+
     def backward_status(self, stream=None) -> int:
         ws = getattr(self, "_bwd_ws", None)
         return lib.moe_check_device_status(ws[:16].view(torch.int32), stream) if ws is not None else 0

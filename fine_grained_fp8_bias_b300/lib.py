@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
     lib.moe_route_workspace_size.argtypes = [I32, I32, I32]
     lib.moe_backward_workspace_size.restype = ctypes.c_size_t
     lib.moe_backward_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
+    lib.moe_wgrad_workspace_size.restype = ctypes.c_size_t
+    lib.moe_wgrad_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
     # Every other entry point returns an int status.  Each one is called only
     # with these argument types: ctypes would otherwise pass Python ints as C
     # int and cut 64-bit pointers to 32 bits.
@@ -89,6 +91,11 @@ def _load() -> ctypes.CDLL:
         "moe_forward_host": [ctypes.POINTER(moe_layer_t), I32, I32, P, P, ctypes.c_float,
                              ctypes.POINTER(moe_batch_buffers_t), P, ctypes.c_size_t, P, P, P],
         "moe_check_device_status": [P, P],
+        "moe_wgrad_ld": [I32, I32],
+        "moe_requant_128x1": [P, P, I32, I32, P, I32, P, P, I32, P, P],
+        "moe_wgrad_gemm_fp8": [P, P, I32, P, P, I32, I32, P, I32, P, P, I32, P, P],
+        "moe_backward_wgrad": [ctypes.POINTER(moe_layer_t), I32, P, P, P, P, ctypes.c_size_t, P,
+                               ctypes.c_size_t, P, ctypes.c_size_t, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -422,3 +429,63 @@ def moe_backward_dgrad(L: moe_layer_t, B: moe_layer_bwd_t, u: torch.Tensor, dh: 
                                    bwd_ws.numel() * bwd_ws.element_size(), _stream(stream)),
            "moe_backward_dgrad")
     return du
+
+
+def moe_wgrad_ld(M: int, G: int) -> int:
+    """Columns of a 128x1 re-quantised operand with M rows in G groups."""
+    return int(_lib.moe_wgrad_ld(M, G))
+
+
+def moe_requant_128x1(q: torch.Tensor, scales: torch.Tensor, group_offsets: torch.Tensor,
+                      ld: Optional[int] = None, status: Optional[torch.Tensor] = None,
+                      stream=None):
+    """q uint8 [M, C] with scales [C/128, M] -> (qt uint8 [C, ld], st float32 [ld/128, C])."""
+    _dev(q, "q")
+    M, C = q.shape
+    G = group_offsets.numel() - 1
+    if ld is None:
+        ld = moe_wgrad_ld(M, G)
+    qt = torch.zeros((C, ld), dtype=torch.uint8, device=q.device)
+    st = torch.zeros((ld // 128, C), dtype=torch.float32, device=q.device)
+    _check(_lib.moe_requant_128x1(_ptr(q), _ptr(scales), M, C, _ptr(group_offsets), G, _ptr(qt),
+                                  _ptr(st), ld, _ptr(status), _stream(stream)), "moe_requant_128x1")
+    return qt, st
+
+
+def moe_wgrad_gemm_fp8(At: torch.Tensor, sAt: torch.Tensor, Bt: torch.Tensor, sBt: torch.Tensor,
+                       group_offsets: torch.Tensor, split: Optional[int] = None,
+                       status: Optional[torch.Tensor] = None, stream=None):
+    """At uint8 [Na, ld], Bt uint8 [Nb, ld] (128x1 layout) -> float32 [G, Na, Nb]
+    (or the two row blocks [G, split, Nb], [G, Na - split, Nb] when split < Na)."""
+    _dev(At, "At")
+    Na, ld = At.shape
+    Nb = Bt.shape[0]
+    G = group_offsets.numel() - 1
+    split = Na if split is None else split
+    out0 = torch.empty((G, split, Nb), dtype=torch.float32, device=At.device)
+    out1 = (torch.empty((G, Na - split, Nb), dtype=torch.float32, device=At.device)
+            if split < Na else None)
+    _check(_lib.moe_wgrad_gemm_fp8(_ptr(At), _ptr(sAt), Na, _ptr(Bt), _ptr(sBt), Nb, ld,
+                                   _ptr(group_offsets), G, _ptr(out0), _ptr(out1), split,
+                                   _ptr(status), _stream(stream)), "moe_wgrad_gemm_fp8")
+    return out0 if out1 is None else (out0, out1)
+
+
+def moe_wgrad_workspace_size(L: moe_layer_t, T: int) -> int:
+    return int(_lib.moe_wgrad_workspace_size(ctypes.byref(L), T))
+
+
+def moe_backward_wgrad(L: moe_layer_t, T: int, fwd_ws: torch.Tensor, bwd_ws: torch.Tensor,
+                       wgrad_ws: torch.Tensor, dW_gate: torch.Tensor, dW_up: torch.Tensor,
+                       dW_down: torch.Tensor, stream=None) -> None:
+    """Weight gradients of every expert for the batch of the last forward and
+    input-gradient calls that used fwd_ws and bwd_ws."""
+    for t, n in ((dW_gate, "dW_gate"), (dW_up, "dW_up"), (dW_down, "dW_down")):
+        _dev(t, n)
+        if t.dtype != torch.float32:
+            raise TypeError(f"{n} must be float32")
+    _check(_lib.moe_backward_wgrad(ctypes.byref(L), T, _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down),
+                                   _ptr(fwd_ws), fwd_ws.numel() * fwd_ws.element_size(),
+                                   _ptr(bwd_ws), bwd_ws.numel() * bwd_ws.element_size(),
+                                   _ptr(wgrad_ws), wgrad_ws.numel() * wgrad_ws.element_size(),
+                                   _stream(stream)), "moe_backward_wgrad")

@@ -336,6 +336,65 @@ int moe_backward_dgrad(const moe_layer_t* L, const moe_layer_bwd_t* B, const uin
                        float* du, void* fwd_ws, size_t fwd_ws_bytes, void* bwd_ws,
                        size_t bwd_ws_bytes, void* stream);
 
+/* Weight gradients (the pages keep FP8 activations in storage and master
+ * weights and gradients in 16/32 bits, [SYH] FP8 資料格式訓練 and [YLY]
+ * §4.3; they wish for transposed GEMMs in hardware, [YLY] hardware
+ * suggestions, because tensors held in 1x128 tiles along features are
+ * contracted over tokens here).  Reading: each FP8 tensor the layer holds is
+ * dequantised (x = dec(q) * s, a float32 product), transposed and
+ * re-quantised in 128x1 tiles: 128 consecutive rows of one group by one
+ * column, scale = amax / 448, code = E4M3(x / scale) (the moe_quant_1x128
+ * rule); a group's last block is ragged and a block never spans two groups.
+ *
+ * Padded layout of a transposed operand with C columns: slab offsets pb[g] =
+ * sum over g' < g of ceil(rows_g' / 128); group g's rows become columns
+ * 128 pb[g] .. of qt [C, ld] (codes past the group's last row are 0), and
+ * the scales st [ld/128, C] hold slab j's C scales contiguously.  ld must be
+ * at least moe_wgrad_ld(M, G) (a multiple of 128 covering any row split). */
+int moe_wgrad_ld(int M, int G);
+
+/* q [M, C] E4M3 codes with scales [C/128][M] (the 1x128 layout of
+ * moe_quant_1x128); group_offsets [G+1] (device) as in moe_grouped_gemm_fp8
+ * (non-decreasing, within [0, M]; otherwise MOE_ERR_BAD_INDEX goes to
+ * status[0] and nothing is written).  Writes qt [C, ld] and st [ld/128, C]
+ * in the padded layout above; columns past the last group's block are not
+ * written.  C a multiple of 128; q, qt 16-byte aligned. */
+int moe_requant_128x1(const uint8_t* q, const float* scales, int M, int C,
+                      const int32_t* group_offsets, int G, uint8_t* qt, float* st, int ld,
+                      int32_t* status, void* stream);
+
+/* Token-contracted FP8 GEMM of the weight gradient: for every group g,
+ *   out_g[n, m] = sum over g's slabs kb of fma(p, sA[kb, n] * sB[kb, m], .)
+ * in float32 (p = the tensor-core sum of the slab's 128 rows; the scale
+ * product is a float32 multiply), i.e. out_g = At_g Bt_g^T over g's rows.
+ *   At [Na, ld], sAt [ld/128, Na]; Bt [Nb, ld], sBt [ld/128, Nb] (padded
+ *   layout of moe_requant_128x1 with the same group_offsets).
+ *   Output rows n < split go to out0 [G, split, Nb], rows n >= split to
+ *   out1 [G, Na - split, Nb] (NULL when split == Na).  A group without rows
+ *   gets zeros.  Na, Nb, split multiples of 128 (0 < split <= Na); ld a
+ *   multiple of 16 covering the padded rows; out pointers 16-byte aligned.
+ * status (device int32 [2], nullable) as in moe_grouped_gemm_fp8. */
+int moe_wgrad_gemm_fp8(const uint8_t* At, const float* sAt, int Na, const uint8_t* Bt,
+                       const float* sBt, int Nb, int ld, const int32_t* group_offsets, int G,
+                       float* out0, float* out1, int split, int32_t* status, void* stream);
+
+/* Workspace bytes moe_backward_wgrad needs for up to T_max tokens (the four
+ * re-quantised operands; 0 if L is invalid). */
+size_t moe_wgrad_workspace_size(const moe_layer_t* L, int T_max);
+
+/* Weight gradients of every expert for the batch of the last moe_forward and
+ * moe_backward_dgrad calls (same L and T; their workspaces are read: the
+ * forward's activation rows A and h, the backward's dy and [dG | dU]).  The
+ * four tensors are re-quantised in 128x1 tiles into wgrad_ws, then
+ *   dW_down [E+S, d, I] = dy^T h   and   [dW_gate ; dW_up] [E+S, 2I, d] =
+ *   [dG | dU]^T A, both float32, written (not accumulated).
+ * Experts that no token selected get zeros.  Device errors go to the status
+ * word of bwd_ws (moe_check_device_status(bwd_ws, stream)).  wgrad_ws:
+ * moe_wgrad_workspace_size(L, T) bytes, 256-byte aligned. */
+int moe_backward_wgrad(const moe_layer_t* L, int T, float* dW_gate, float* dW_up, float* dW_down,
+                       void* fwd_ws, size_t fwd_ws_bytes, void* bwd_ws, size_t bwd_ws_bytes,
+                       void* wgrad_ws, size_t wgrad_ws_bytes, void* stream);
+
 /* Auxiliary-loss-free bias update at the end of a step ([TH] Method §2:
  * b_i -= gamma when expert i is overloaded, += gamma when underloaded;
  * gamma = 0.001 there).  With n = T*K selections, expert e is overloaded when
