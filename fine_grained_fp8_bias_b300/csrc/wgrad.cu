@@ -82,75 +82,168 @@ __device__ bool warp_slab_offsets(const int32_t* go, int G, int M, int* pb, int3
     return !bad;
 }
 
-// One block per (128-column block cb, padded slab j): 128 rows of group g by
-// 128 columns in, 128 columns x 128 rows out.
-__global__ void __launch_bounds__(256) requant_128x1_kernel(const uint8_t* __restrict__ q,
-                                                            const float* __restrict__ s, int M, int C,
-                                                            const int32_t* __restrict__ go, int G,
-                                                            uint8_t* __restrict__ qt,
-                                                            float* __restrict__ st, int ld,
-                                                            int32_t* status) {
-    __shared__ int pb[kMaxGroups + 1];
-    __shared__ __align__(16) uint8_t tile[128][128 + 16];   // [row][column]
-    __shared__ uint32_t tq[128][33];                        // [column][row / 4], 4 codes a word
-    __shared__ float rs[128];
-    __shared__ float part[2][128];
-    __shared__ int ok_flag;
+// Shared memory of the re-quantisation kernel (dynamic: above 48 KB).
+struct RqSmem {
+    uint8_t tile[2][128][128];          // double-buffered input tile [row][column]
+    uint32_t tq[128][33];               // output tile [column][row / 4], 4 codes a word
+    float part[8][128];                 // column amax of each warp's 16 rows
+    int pb[kMaxGroups + 1];
+    float rs[2][128];                   // row scales of each buffer
+    int ok;
+};
+
+// x / scale correctly rounded, from r = RN(1 / scale), with no division:
+// y = RN(x r) is within 2 ulps of the quotient; one correction step
+// q1 = RN(y + RN(x - scale y) r) makes it faithful (within 1 ulp), and a
+// second step from a faithful quotient with the correctly rounded reciprocal
+// gives the correctly rounded quotient (Markstein, IBM J. Res. Dev. 34(1),
+// 1990; the residual x - scale q1 is exact in one FMA).  The correction sums
+// turn a -0 quotient into +0, so the sign is taken from x.  Valid for finite x
+// and scale >= 2^-100 (no underflow in the residuals that matters: a quotient
+// below 2^-10 encodes to 0 whatever its last bits).
+__device__ __forceinline__ float div_rn_rcp(float x, float scale, float r) {
+    const float y = x * r;
+    const float q1 = fmaf(fmaf(-scale, y, x), r, y);
+    const float q2 = fmaf(fmaf(-scale, q1, x), r, q1);
+    return copysignf(q2, x);
+}
+
+// One block per padded slab j (128 rows of one group) and a stride of
+// 128-column blocks: the group lookup is paid once, then the column blocks
+// stream through a two-deep cp.async ring (load of block k+1 in flight while
+// block k is converted and written).  Thread (warp w, lane l) converts the
+// four columns 4l .. 4l + 3 of rows 16 w .. 16 w + 15: one 32-bit shared
+// load brings a row's four codes.
+__global__ void __launch_bounds__(256, 4) requant_128x1_kernel(const uint8_t* __restrict__ q,
+                                                               const float* __restrict__ s, int M,
+                                                               int C, const int32_t* __restrict__ go,
+                                                               int G, uint8_t* __restrict__ qt,
+                                                               float* __restrict__ st, int ld,
+                                                               int32_t* status) {
+    extern __shared__ __align__(16) uint8_t rq_raw[];
+    RqSmem& sm = *reinterpret_cast<RqSmem*>(rq_raw);
     const int tid = threadIdx.x;
-    const int cb = blockIdx.x, j = blockIdx.y;
+    const int j = blockIdx.y;
+    const int ncb = C / 128;
+    // the group offsets through shared memory (one coalesced read), then the scan
+    int* gos = reinterpret_cast<int*>(&sm.tq[0][0]);      // tq is free until the first block
+    for (int g = tid; g <= G; g += 256) gos[g] = go[g];
+    __syncthreads();
     if (tid < 32) {
-        const bool ok = warp_slab_offsets(go, G, M, pb, status);
-        if (tid == 0) ok_flag = ok;
+        const bool ok = warp_slab_offsets(gos, G, M, sm.pb, status);
+        if (tid == 0) sm.ok = ok;
     }
     __syncthreads();
-    if (!ok_flag || j >= pb[G]) return;
-    if (pb[G] > ld / 128) {                  // the padded rows do not fit the output
+    if (!sm.ok || j >= sm.pb[G]) return;
+    if (sm.pb[G] > ld / 128) {               // the padded rows do not fit the output
         if (tid == 0) flag_status(status, MOE_ERR_BAD_INDEX);
         return;
     }
     int lo = 0, hi = G;                      // pb[lo] <= j < pb[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (pb[mid] <= j) lo = mid; else hi = mid;
+        if (sm.pb[mid] <= j) lo = mid; else hi = mid;
     }
-    const int r0 = go[lo] + (j - pb[lo]) * 128;
-    const int n = min(128, go[lo + 1] - r0);
-    // rows r0 .. r0 + n - 1, columns 128 cb ..; rows past n are zero
-    for (int i = tid; i < 128 * 8; i += 256) {
-        const int r = i >> 3, c16 = (i & 7) * 16;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < n) v = *reinterpret_cast<const uint4*>(q + (size_t)(r0 + r) * C + (size_t)cb * 128 + c16);
-        *reinterpret_cast<uint4*>(&tile[r][c16]) = v;
-    }
-    if (tid < 128) rs[tid] = tid < n ? s[(size_t)cb * M + r0 + tid] : 0.0f;
-    __syncthreads();
-    // thread (c, h): column c, rows 64 h .. 64 h + 63
-    const int c = tid & 127, h = tid >> 7;
-    float x[64];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-        const int r = 64 * h + i;
-        const uint16_t pair = static_cast<uint16_t>(tile[r][c] | (tile[r + 1][c] << 8));
-        const float2 f = e4m3x2_to_f32(pair);
-        x[i] = __fmul_rn(f.x, rs[r]);
-        x[i + 1] = __fmul_rn(f.y, rs[r + 1]);
-        amax = fmaxf(amax, fmaxf(fabsf(x[i]), fabsf(x[i + 1])));
-    }
-    part[h][c] = amax;
-    __syncthreads();
-    amax = fmaxf(part[0][c], part[1][c]);
-    const float scale = tile_scale(amax);
-#pragma unroll
-    for (int i = 0; i < 64; i += 4)
-        tq[c][16 * h + i / 4] = amax == 0.0f ? 0u : quant4(x[i], x[i + 1], x[i + 2], x[i + 3], scale);
-    if (h == 0) st[(size_t)j * C + (size_t)cb * 128 + c] = scale;
-    __syncthreads();
-    // row c of the output tile: 128 codes, one coalesced 128-byte write per warp
+    const int r0 = gos[lo] + (j - sm.pb[lo]) * 128;
+    const int n = min(128, gos[lo + 1] - r0);
+    __syncthreads();                         // gos (in tq) is read by all before tq is reused
+
+    // rows r0 .. r0 + n - 1 of column block cb into buffer b; rows past n are zero
+    auto stage = [&](int cb, int b) {
+        for (int i = tid; i < 128 * 8; i += 256) {
+            const int r = i >> 3, c16 = (i & 7) * 16;
+            const bool v = r < n;
+            cp_async16(&sm.tile[b][r][c16], v ? q + (size_t)(r0 + r) * C + (size_t)cb * 128 + c16 : q,
+                       v ? 16u : 0u);
+        }
+        if (tid < 128) {
+            const bool v = tid < n;
+            cp_async4(&sm.rs[b][tid], v ? s + (size_t)cb * M + r0 + tid : s, v ? 4u : 0u);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
     const int warp = tid >> 5, lane = tid & 31;
-    for (int cc = warp; cc < 128; cc += 8)
-        *reinterpret_cast<uint32_t*>(qt + (size_t)(cb * 128 + cc) * ld + (size_t)j * 128 + lane * 4) =
-            tq[cc][lane];
+    const int c0 = 4 * lane, rw = 16 * warp;
+    // x = dec(code) * row scale for row r, columns c0 .. c0 + 3
+    auto deq = [&](int b, int r, float (&x)[4]) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(&sm.tile[b][r][c0]);
+        const float2 f0 = e4m3x2_to_f32(static_cast<uint16_t>(w & 0xFFFFu));
+        const float2 f1 = e4m3x2_to_f32(static_cast<uint16_t>(w >> 16));
+        const float sr = sm.rs[b][r];
+        x[0] = __fmul_rn(f0.x, sr);
+        x[1] = __fmul_rn(f0.y, sr);
+        x[2] = __fmul_rn(f1.x, sr);
+        x[3] = __fmul_rn(f1.y, sr);
+    };
+    int cb = blockIdx.x;
+    if (cb < ncb) stage(cb, 0);
+    for (int k = 0; cb < ncb; ++k, cb += gridDim.x) {
+        const int b = k & 1;
+        const bool more = cb + (int)gridDim.x < ncb;
+        if (more) stage(cb + gridDim.x, b ^ 1);
+        if (more) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        // pass 1: column amax over this warp's 16 rows, then over the 8 warps
+        float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            float x[4];
+            deq(b, rw + i, x);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) am[t] = fmaxf(am[t], fabsf(x[t]));
+        }
+        *reinterpret_cast<float4*>(&sm.part[warp][c0]) = make_float4(am[0], am[1], am[2], am[3]);
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float4 v = *reinterpret_cast<const float4*>(&sm.part[w][c0]);
+            am[0] = fmaxf(am[0], v.x);
+            am[1] = fmaxf(am[1], v.y);
+            am[2] = fmaxf(am[2], v.z);
+            am[3] = fmaxf(am[3], v.w);
+        }
+        float sc[4], rc[4];
+        bool all_fast = true;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            sc[t] = tile_scale(am[t]);
+            rc[t] = __frcp_rn(sc[t]);
+            all_fast = all_fast && sc[t] >= 0x1p-100f;
+        }
+        if (warp == 0)
+            *reinterpret_cast<float4*>(st + (size_t)j * C + (size_t)cb * 128 + c0) =
+                make_float4(sc[0], sc[1], sc[2], sc[3]);
+        // pass 2: four rows at a time; column t's four codes make one word of tq
+        // (an all-zero column gets code 0); IEEE division for scales near underflow
+        auto pass2 = [&](auto div) {
+#pragma unroll 1
+            for (int i = 0; i < 16; i += 4) {
+                float x[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) deq(b, rw + i + u, x[u]);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    float y[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) y[u] = div(x[u][t], t);
+                    const uint32_t word = static_cast<uint32_t>(e4m3x2(y[0], y[1])) |
+                                          (static_cast<uint32_t>(e4m3x2(y[2], y[3])) << 16);
+                    sm.tq[c0 + t][(rw + i) >> 2] = am[t] != 0.0f ? word : 0u;
+                }
+            }
+        };
+        if (all_fast)
+            pass2([&](float v, int t) { return div_rn_rcp(v, sc[t], rc[t]); });
+        else
+            pass2([&](float v, int t) { return __fdiv_rn(v, sc[t]); });
+        __syncthreads();
+        // row cc of the output tile: 128 codes, one coalesced 128-byte write per warp
+        for (int cc = warp; cc < 128; cc += 8)
+            *reinterpret_cast<uint32_t*>(qt + (size_t)(cb * 128 + cc) * ld + (size_t)j * 128 + lane * 4) =
+                sm.tq[cc][lane];
+        __syncthreads();                     // tq, part and buffer b are reused next round
+    }
 }
 
 // -------------------------------------------------------------- the GEMM
@@ -519,8 +612,17 @@ int launch_requant_128x1(const uint8_t* q, const float* s, int M, int C, const i
     if (M == 0 || G == 0 || C == 0) return MOE_OK;
     const long long slabs = ((long long)M + 127LL * G) / 128 + 1;
     if (slabs > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
-    requant_128x1_kernel<<<dim3(C / 128, (unsigned)slabs), 256, 0, stream>>>(q, s, M, C, go, G, qt, st,
-                                                                          ld, status);
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(requant_128x1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(RqSmem));
+    });
+    // about four blocks per column block stride: enough slabs x strides to fill
+    // the SMs while each block amortises its group lookup over several blocks
+    const int ncb = C / 128;
+    const int stride = ncb < 8 ? ncb : 8;
+    requant_128x1_kernel<<<dim3(stride, (unsigned)slabs), 256, sizeof(RqSmem), stream>>>(
+        q, s, M, C, go, G, qt, st, ld, status);
     return check_launch();
 }
 
