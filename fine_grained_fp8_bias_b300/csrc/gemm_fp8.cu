@@ -135,17 +135,18 @@ __device__ __forceinline__ Tile find_tile(const Ctl* ctl, int G, int tile) {
     return Tile{lo, local / mtiles, local % mtiles};
 }
 
-// x / scale for |x| <= 448 scale: with r = RN(1 / scale) and y = RN(x r), the
-// residual x - scale y is exact in one FMA, and RN(y + residual r) (one
-// Markstein correction step, 1990) gives the correctly rounded quotient
-// except in rare near-halfway cases, where it is one float32 ulp off; a
-// quotient that is exactly representable, such as an E4M3 tie point, is
-// always returned exactly.  The sum in the correction turns a -0 quotient
-// into +0, so the sign is taken from x (scale > 0).  The scale must be far
-// from underflow.
+// x / scale correctly rounded (the IEEE quotient) without a division
+// instruction, from r = RN(1 / scale): y = RN(x r) is within 2 ulps of the
+// quotient; one correction step q1 = RN(y + RN(x - scale y) r) makes it
+// faithful, and a second step from a faithful quotient with the correctly
+// rounded reciprocal rounds correctly (Markstein, IBM J. Res. Dev. 34(1),
+// 1990; the residual x - scale q1 is exact in one FMA).  The correction sums
+// turn a -0 quotient into +0, so the sign is taken from x (scale > 0).  The
+// scale must be far from underflow.
 __device__ __forceinline__ float div_rcp(float x, float scale, float r) {
     const float y = x * r;
-    return copysignf(fmaf(fmaf(-scale, y, x), r, y), x);
+    const float q1 = fmaf(fmaf(-scale, y, x), r, y);
+    return copysignf(fmaf(fmaf(-scale, q1, x), r, q1), x);
 }
 __device__ __forceinline__ uint32_t quant4_rcp(float a, float b, float c, float d, float scale,
                                                float r) {

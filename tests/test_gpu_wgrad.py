@@ -59,6 +59,28 @@ def test_requant_128x1_bit_exact(L, orc):
         assert np.array_equal(st[pb[g]:pb[g + 1]].T, rs), f"group {g}"
 
 
+def test_requant_128x1_many_quotients(L, orc):
+    # 4 M quotients over scales spanning 2^-90 .. 2^20: the division-free
+    # quotient must match the oracle's IEEE division everywhere
+    rng = np.random.default_rng(31)
+    sizes = [1000, 1, 2047, 129, 823]
+    go = _offsets(sizes)
+    M, C = int(go[-1]), 1024
+    q = _codes(rng, (M, C))
+    s = (rng.uniform(1.0, 2.0, size=(M, C // 128)) *
+         2.0 ** rng.integers(-90, 20, size=(M, C // 128))).astype(np.float32)
+    qt, st = L.moe_requant_128x1(torch.from_numpy(q).cuda(), torch.from_numpy(s.T.copy()).cuda(),
+                                 torch.from_numpy(go).cuda())
+    torch.cuda.synchronize()
+    qt, st = qt.cpu().numpy(), st.cpu().numpy()
+    pb = _pb(sizes)
+    for g in range(len(sizes)):
+        rq, rs = orc.requant_128x1(q[go[g]:go[g + 1]], s[go[g]:go[g + 1]])
+        cols = slice(128 * pb[g], 128 * pb[g + 1])
+        assert np.array_equal(qt[:, cols], rq), f"group {g}"
+        assert np.array_equal(st[pb[g]:pb[g + 1]].T, rs), f"group {g}"
+
+
 def _wgrad_case(rng, integers, orc):
     go = _offsets(SIZES)
     G = len(SIZES)
