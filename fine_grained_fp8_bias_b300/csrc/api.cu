@@ -306,9 +306,9 @@ int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, i
         const cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    if ((rc = launch_route_tc(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
-                              counts, route_ws, status, st, L->n_groups, L->topk_groups,
-                              L->group_topk)))
+    if ((rc = launch_route_layer(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
+                                 counts, route_ws, status, st, L->n_groups, L->topk_groups,
+                                 L->group_topk)))
         return rc;
     if (T == 0) return MOE_OK;
     if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,

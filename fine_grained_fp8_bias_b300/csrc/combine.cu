@@ -18,8 +18,9 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], uint4 raw, float w) 
     }
 }
 
-// One block per token (grid-stride); each thread owns 8 consecutive columns
-// per step.  Sum order: u, shared experts, routed experts by slot.  gate NULL:
+// One work item = one token's chunk of 8 * blockDim columns (grid-stride), so
+// a few tokens still spread over many blocks; each thread owns 8 consecutive
+// columns.  Sum order: u, shared experts, routed experts by slot.  gate NULL:
 // every routed row has weight 1 (the input gradient's gather).
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ u,
                                                       const uint16_t* __restrict__ Y,
@@ -30,14 +31,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       float* __restrict__ h) {
     __shared__ int rows[kMaxTopK];
     __shared__ float gs[kMaxTopK];
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const int chunk = blockDim.x * 8;
+    const int nch = (d + chunk - 1) / chunk;
+    const long long items = (long long)T * nch;
+    for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+        const int t = (int)(item / nch);
         __syncthreads();
         if (threadIdx.x < K) {
             rows[threadIdx.x] = inv_row[(size_t)t * K + threadIdx.x];
             gs[threadIdx.x] = gate ? gate[(size_t)t * K + threadIdx.x] : 1.0f;
         }
         __syncthreads();
-        for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+        {
+            const int c = (int)(item % nch) * chunk + threadIdx.x * 8;
+            if (c >= d) continue;
             float acc[8];
             const uint4 ur = *reinterpret_cast<const uint4*>(u + (size_t)t * d + c);
 #pragma unroll
@@ -70,9 +77,9 @@ __global__ void update_bias_kernel(const int32_t* __restrict__ counts, int E, lo
 int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
                    const uint16_t* Ysh, int T, int d, int K, int S, float* h, cudaStream_t st) {
     if (T == 0) return MOE_OK;
-    int threads = 128;
-    while (threads < 256 && threads * 8 < d) threads *= 2;
-    const int blocks = T < 148 * 16 ? T : 148 * 16;
+    const int threads = 128;
+    const long long items = (long long)T * ((d + threads * 8 - 1) / (threads * 8));
+    const int blocks = (int)(items < 148 * 16 ? items : 148 * 16);
     combine_kernel<<<blocks, threads, 0, st>>>(u, Y, gate, inv_row, Ysh, T, d, K, S, h);
     return check_launch();
 }

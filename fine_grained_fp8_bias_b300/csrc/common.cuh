@@ -52,9 +52,12 @@ int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_ro
                           uint8_t* q, float* scales, int scale_ld, int32_t* status,
                           cudaStream_t st);
 int launch_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales, cudaStream_t st);
+// CUDA-core router (route.cu).  part (nullable): room for split-K partial
+// logits (part_floats floats), summed in a fixed order; without it the
+// partials are added atomically into logits.
 int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                  int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
-                 cudaStream_t st);
+                 cudaStream_t st, float* part = nullptr, size_t part_floats = 0);
 // The tensor-core router of moe_route (route_tc.cu): workspace bytes for T
 // tokens, and the launch (the workspace's first int32 is not touched; the
 // status word is passed separately).
@@ -63,6 +66,12 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
                     int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
                     int32_t* status, cudaStream_t st, int n_groups = 0, int topk_groups = 0,
                     int group_topk = 0);
+// The layer's router: the CUDA-core exact router for small batches without
+// group limits, else launch_route_tc (same workspace as launch_route_tc).
+int launch_route_layer(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
+                       int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
+                       int32_t* status, cudaStream_t st, int n_groups, int topk_groups,
+                       int group_topk);
 // The router's logit estimates summed into out [T, E], and the bound's
 // centroid norms of the bound into norms_out [E] (device), for checking the bound.
 int launch_route_estimate(const uint16_t* u, const float* cent, int T, int d, int E, float* out,

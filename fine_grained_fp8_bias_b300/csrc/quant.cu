@@ -85,8 +85,14 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const int warps_per_block = blockDim.x >> 5;
     const int half = lane >> 4;
     const int hl = lane & 15;
-    for (int t = blockIdx.x * warps_per_block + (threadIdx.x >> 5); t < T;
-         t += gridDim.x * warps_per_block) {
+    // one work item = one token's 256-column chunk (two 1x128 tiles), so a
+    // few tokens still spread over many warps
+    const int nch = (d + 255) / 256;
+    const long long items = (long long)T * nch;
+    for (long long item = (long long)blockIdx.x * warps_per_block + (threadIdx.x >> 5); item < items;
+         item += (long long)gridDim.x * warps_per_block) {
+        const int t = (int)(item / nch);
+        const int c0 = (int)(item % nch) * 256;
         // lane j < K holds routed row j of this token, lane K + s shared row s
         int my_row = -1;
         if (lane < K) {
@@ -100,7 +106,7 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
         }
         const int R = K + S;
         const uint16_t* xr = x + (size_t)t * d;
-        for (int c0 = 0; c0 < d; c0 += 256) {
+        {
             const int col = c0 + half * 128 + hl * 8;
             const bool active = col < d;
             float v[8];
@@ -194,8 +200,8 @@ int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_ro
                           cudaStream_t st) {
     if (T == 0) return MOE_OK;
     const int warps = 8;
-    int blocks = (T + warps - 1) / warps;
-    if (blocks > 148 * 16) blocks = 148 * 16;
+    const long long items = (long long)T * ((d + 255) / 256);
+    const int blocks = (int)((items + warps - 1) / warps < 148 * 16 ? (items + warps - 1) / warps : 148 * 16);
     quant_dispatch_kernel<<<blocks, warps * 32, 0, st>>>(x, T, d, inv_row, K, S, T * (K + S), q,
                                                           scales, scale_ld, status);
     return check_launch();

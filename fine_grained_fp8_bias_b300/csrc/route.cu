@@ -42,10 +42,13 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
 // the chunk is then added into the running sum with TwoSum, and the
 // rounding errors are kept in a separate compensation term (so only the
 // short chains round inexactly).  With split > 1 (few tokens) every block
-// adds its partial sum atomically into a zeroed l.
+// writes its partial sum to part[split index][t][e] (the selection kernel adds
+// them in a fixed order), or, without a partial buffer, adds it atomically
+// into a zeroed l (the sum's last bits then depend on the arrival order).
 __global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict__ u,
                                                      const float* __restrict__ c, int T, int d,
-                                                     int E, int split, float* __restrict__ l) {
+                                                     int E, int split, float* __restrict__ l,
+                                                     float* __restrict__ part) {
     __shared__ __align__(16) float us[LK][LT];
     __shared__ __align__(16) float cs[LK][LE];
     const int tid = threadIdx.x;
@@ -125,11 +128,71 @@ __global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict_
             const int e = e0 + tx * 4 + j;
             if (e >= E) continue;
             const float v = acc[i][j] + cmp[i][j];
-            if (split > 1)
-                atomicAdd(&l[(size_t)t * E + e], v);
-            else
+            if (split == 1)
                 l[(size_t)t * E + e] = v;
+            else if (part)
+                part[((size_t)blockIdx.z * T + t) * E + e] = v;
+            else
+                atomicAdd(&l[(size_t)t * E + e], v);
         }
+    }
+}
+
+// Few tokens (T <= kSmallT): one warp per expert computes that expert's logit
+// for every token, streaming the centroid row once with all its loads in
+// flight.  Lane L holds columns 128 c + 4 L .. + 3 of every 128-column chunk c;
+// each 8-chunk run (32 products per lane and token) is a plain FMA chain,
+// added with TwoSum, and the lanes' sums are combined by a TwoSum butterfly
+// (every lane ends with the same value).  No split partials, no atomics.
+constexpr int kSmallT = 8;
+__global__ void __launch_bounds__(128) logits_small_kernel(const uint16_t* __restrict__ u,
+                                                           const float* __restrict__ c, int T,
+                                                           int d, int E, float* __restrict__ l) {
+    const int e = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (e >= E) return;
+    const float* crow = c + (size_t)e * d + lane * 4;
+    float acc[kSmallT], cmp[kSmallT], chain[kSmallT];
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t) acc[t] = cmp[t] = chain[t] = 0.0f;
+    const int nch = d / 128;
+    for (int c0 = 0; c0 < nch; c0 += 8) {
+        const int n = min(8, nch - c0);
+        float4 cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < n) cv[i] = *reinterpret_cast<const float4*>(crow + (size_t)(c0 + i) * 128);
+#pragma unroll
+        for (int t = 0; t < kSmallT; ++t) {
+            if (t >= T) break;
+            const uint16_t* ur = u + (size_t)t * d + lane * 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i >= n) break;
+                const uint2 w = *reinterpret_cast<const uint2*>(ur + (size_t)(c0 + i) * 128);
+                chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu)), cv[i].x, chain[t]);
+                chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16)), cv[i].y, chain[t]);
+                chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu)), cv[i].z, chain[t]);
+                chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16)), cv[i].w, chain[t]);
+            }
+            float err;
+            acc[t] = two_sum(acc[t], chain[t], err);
+            cmp[t] += err;
+            chain[t] = 0.0f;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t) {
+        if (t >= T) break;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oa = __shfl_xor_sync(0xffffffffu, acc[t], off);
+            const float oc = __shfl_xor_sync(0xffffffffu, cmp[t], off);
+            float err;
+            acc[t] = two_sum(acc[t], oa, err);
+            cmp[t] = (cmp[t] + oc) + err;
+        }
+        if (lane == 0) l[(size_t)t * E + e] = acc[t] + cmp[t];
     }
 }
 
@@ -139,8 +202,11 @@ __device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
 }
 
 // One warp per token.  Lane L holds experts L, L + 32, ... (NV per lane).
+// With part != NULL the logit is the sum of the split partials, added in
+// split order with TwoSum compensation.
 template <int NV>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ l,
+                                                   const float* __restrict__ part, int split,
                                                    const float* __restrict__ bias, int T, int E,
                                                    int K, int32_t* __restrict__ idx,
                                                    float* __restrict__ gate,
@@ -154,7 +220,27 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ l,
     for (int j = 0; j < NV; ++j) {
         const int e = j * 32 + lane;
         if (e < E) {
-            const float x = l[(size_t)t * E + e];
+            float x;
+            if (part) {
+                // eight partials loaded at a time, then added in split order
+                float acc = 0.0f, cmp = 0.0f;
+                for (int z0 = 0; z0 < split; z0 += 8) {
+                    float v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = z0 + i < split ? part[((size_t)(z0 + i) * T + t) * E + e] : 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (z0 + i >= split) break;
+                        float err;
+                        acc = two_sum(acc, v[i], err);
+                        cmp += err;
+                    }
+                }
+                x = acc + cmp;
+            } else {
+                x = l[(size_t)t * E + e];
+            }
             s[j] = __fdiv_rn(1.0f, 1.0f + expf(-x));
             z[j] = s[j] + bias[e];
         } else {
@@ -204,41 +290,52 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ l,
 }
 
 template <int NV>
-void launch_topk_nv(const float* l, const float* bias, int T, int E, int K, int32_t* idx,
-                    float* gate, uint8_t* tie, int32_t* counts, cudaStream_t st) {
+void launch_topk_nv(const float* l, const float* part, int split, const float* bias, int T, int E,
+                    int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts,
+                    cudaStream_t st) {
     const int warps = 8;
-    topk_kernel<NV><<<(T + warps - 1) / warps, warps * 32, 0, st>>>(l, bias, T, E, K, idx, gate,
-                                                                     tie, counts);
+    topk_kernel<NV><<<(T + warps - 1) / warps, warps * 32, 0, st>>>(l, part, split, bias, T, E, K,
+                                                                     idx, gate, tie, counts);
 }
 
 }  // namespace
 
 int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                  int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
-                 cudaStream_t st) {
+                 cudaStream_t st, float* part, size_t part_floats) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (e != cudaSuccess) return cuda_fail(e);
     if (T == 0) return MOE_OK;
     int rc;
-    {
-        const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
-        int split = 1;
+    const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
+    int split = 1;
+    if (T <= kSmallT) {
+        logits_small_kernel<<<(E + 3) / 4, 128, 0, st>>>(u, cent, T, d, E, logits);
+        if ((rc = check_launch())) return rc;
+        part = nullptr;
+    } else {
         const int target = 2 * 148;
         while (gx * gy * split < target && split * 2 <= d / LK / 4) split *= 2;
-        if (split > 1) {
+        // with a partial buffer, as many splits as it holds (a fixed summation order)
+        if (part)
+            while (split > 1 && (size_t)split * T * E > part_floats) split /= 2;
+        const bool use_part = part && split > 1;
+        if (split > 1 && !use_part) {
             e = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
             if (e != cudaSuccess) return cuda_fail(e);
         }
-        logits_kernel<<<dim3(gx, gy, split), 256, 0, st>>>(u, cent, T, d, E, split, logits);
+        logits_kernel<<<dim3(gx, gy, split), 256, 0, st>>>(u, cent, T, d, E, split, logits,
+                                                             use_part ? part : nullptr);
         if ((rc = check_launch())) return rc;
+        if (!use_part) part = nullptr;
     }
     const int nv = (E + 31) / 32;
-    if (nv <= 1) launch_topk_nv<1>(logits, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 2) launch_topk_nv<2>(logits, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 4) launch_topk_nv<4>(logits, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 8) launch_topk_nv<8>(logits, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 16) launch_topk_nv<16>(logits, bias, T, E, K, idx, gate, tie, counts, st);
-    else launch_topk_nv<32>(logits, bias, T, E, K, idx, gate, tie, counts, st);
+    if (nv <= 1) launch_topk_nv<1>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 2) launch_topk_nv<2>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 4) launch_topk_nv<4>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 8) launch_topk_nv<8>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    else if (nv <= 16) launch_topk_nv<16>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    else launch_topk_nv<32>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
     return check_launch();
 }
 

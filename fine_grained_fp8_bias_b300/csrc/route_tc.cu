@@ -904,6 +904,33 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
 
 size_t route_ws_bytes(int T, int d, int E) { return route_ws(T, d, E).total; }
 
+// Below this many tokens the layer routes with the CUDA-core router (all E
+// logits summed exactly, launch_route): the tensor-core screen's fixed costs
+// (centroid split, estimate, one refinement block per token) exceed the
+// exact sums there (measured on B300, V3 decode shapes: 25-36 us against
+// 42-55 us for T <= 128; equal near T = 256).
+constexpr int kSmallRouteT = 256;
+
+int launch_route_layer(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
+                       int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
+                       int32_t* status, cudaStream_t st, int n_groups, int topk_groups,
+                       int group_topk) {
+    const RouteWs w = route_ws(T, d, E);
+    if (n_groups == 0 && T > 0 && T < kSmallRouteT && (size_t)T * E * 4 <= (size_t)E * d * 2) {
+        // the logits [T, E] and the split partials go where the tensor-core path
+        // keeps its centroid pieces and partial estimates
+        char* base = static_cast<char*>(ws);
+        float* logits = reinterpret_cast<float*>(base + w.hi);
+        const size_t part_at = align_up(w.hi + sizeof(float) * (size_t)T * E, 256);
+        float* part = reinterpret_cast<float*>(base + part_at);
+        const size_t part_floats = (w.total - part_at) / sizeof(float);
+        return launch_route(u, cent, bias, T, d, E, K, idx, gate, tie, counts, logits, st, part,
+                            part_floats);
+    }
+    return launch_route_tc(u, cent, bias, T, d, E, K, idx, gate, tie, counts, ws, status, st,
+                           n_groups, topk_groups, group_topk);
+}
+
 int launch_gate_term(const uint16_t* u, const uint16_t* dh, const uint16_t* Y, const int32_t* inv_row,
                      const int32_t* idx, const float* gate, const float* cent, int T, int d, int K,
                      int M, float* du, int32_t* status, cudaStream_t st) {

@@ -69,8 +69,10 @@ def test_v3_prefill_sampled(orc):
     check_layer(orc, wl.V3_PREFILL, tokens=[0, 4095])
 
 
-@pytest.mark.parametrize("T", [1, 16])
+@pytest.mark.parametrize("T", [1, 16, 64, 255, 256])
 def test_v3_decode(orc, T):
+    # below 256 tokens the layer routes with the CUDA-core exact router, from 256 on
+    # with the tensor-core screen
     cfg = wl.V3_DECODE.with_(T=T)
     check_layer(orc, cfg, tokens=[0, T - 1] if T > 1 else [0])
 
@@ -104,6 +106,23 @@ def test_forward_is_deterministic():
     b = L.forward(u)
     torch.cuda.synchronize()
     assert torch.equal(h1, b["h"])
+
+
+@pytest.mark.parametrize("T", [1, 16, 200])
+def test_small_batch_forward_is_deterministic(T):
+    # the small-batch router sums its split partial logits in a fixed order
+    from fine_grained_fp8_bias_b300.layer import MoELayer
+    cfg = wl.V3_DECODE.with_(T=T)
+    L = MoELayer.from_config(wl.TINY.with_(d=1024, E=64, K=6), "cuda")
+    u = wl.tokens(cfg.with_(d=1024), "cuda")
+    outs = []
+    for _ in range(3):
+        o = L.forward(u)
+        outs.append({k: v.clone() for k, v in o.items()})
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        for k in ("h", "idx", "gate", "tie", "counts"):
+            assert torch.equal(o[k], outs[0][k]), k
 
 
 @pytest.mark.parametrize("name,n", [("tiny", 5), ("ragged", 4)])
