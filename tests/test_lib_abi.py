@@ -116,3 +116,45 @@ def test_workspace_size_and_layer_checks(lib):
     # workspace smaller than required
     assert L.moe_forward(ctypes.byref(layer), 1 << 20, 4096, 1 << 20, 1 << 20, 1 << 20, 1 << 20,
                          1 << 20, 1 << 20, 1024, None) == -6
+
+
+def test_backward_entry_points_validate_on_the_host(lib):
+    L = lib.lib()
+    fake = 1 << 20                     # never dereferenced: every call below fails validation
+    # padded column count of the 128x1 form: M + 127 G rounded up to 128
+    assert L.moe_wgrad_ld(36864, 257) == (36864 + 127 * 257 + 127) // 128 * 128
+    assert L.moe_wgrad_ld(1, 1) == 128 and L.moe_wgrad_ld(0, 5) == 640 and L.moe_wgrad_ld(-1, 1) == 0
+    # re-quantisation: C not a multiple of 128, ld not a multiple of 16, null or misaligned buffers
+    assert L.moe_requant_128x1(fake, fake, 300, 100, fake, 4, fake, fake, 1024, None, None) == -2
+    assert L.moe_requant_128x1(fake, fake, 300, 128, fake, 4, fake, fake, 1000, None, None) == -2
+    assert L.moe_requant_128x1(fake, None, 300, 128, fake, 4, fake, fake, 1024, None, None) == -1
+    assert L.moe_requant_128x1(fake + 8, fake, 300, 128, fake, 4, fake, fake, 1024, None, None) == -3
+    assert L.moe_requant_128x1(fake, fake, 0, 128, fake, 4, fake, fake, 1024, None, None) == 0
+    # token-contracted GEMM: sizes, split, the second output, alignment
+    assert L.moe_wgrad_gemm_fp8(fake, fake, 100, fake, fake, 128, 1024, fake, 4, fake, None, 100,
+                                None, None) == -2
+    assert L.moe_wgrad_gemm_fp8(fake, fake, 256, fake, fake, 128, 1024, fake, 4, fake, None, 384,
+                                None, None) == -1
+    assert L.moe_wgrad_gemm_fp8(fake, fake, 256, fake, fake, 128, 1024, fake, 4, fake, None, 128,
+                                None, None) == -1
+    assert L.moe_wgrad_gemm_fp8(fake, fake, 256, fake, fake, 128, 1024, fake, 4, fake + 8, fake, 128,
+                                None, None) == -3
+    assert L.moe_wgrad_gemm_fp8(fake, fake, 256, fake, fake, 128, 1024, fake, 0, fake, fake, 128,
+                                None, None) == 0
+    # layer-level backward: workspace sizes, a missing transposed-weight set, short or misaligned workspaces
+    layer = lib.moe_layer_t(7168, 256, 8, 1, 2048, *([1 << 20] * 8))
+    T = 4096
+    nb = L.moe_backward_workspace_size(ctypes.byref(layer), T)
+    nw = L.moe_wgrad_workspace_size(ctypes.byref(layer), T)
+    M, ld = T * 9, L.moe_wgrad_ld(T * 9, 257)
+    assert nb >= M * 7168 + 2 * M * 2048 + M * 2 * 2048 + 2 * M * 7168
+    assert nw >= ld * (2 * 7168 + 2048 + 2 * 2048)
+    nf = L.moe_workspace_size(ctypes.byref(layer), T)
+    assert L.moe_backward_dgrad(ctypes.byref(layer), None, fake, fake, T, fake, fake, fake, fake, nf,
+                                fake, nb, None) == -1
+    assert L.moe_backward_wgrad(ctypes.byref(layer), T, fake, fake, fake, fake, nf, fake, nb, fake,
+                                nw - 256, None) == -6
+    assert L.moe_backward_wgrad(ctypes.byref(layer), T, fake, fake, fake, fake, nf, fake, nb,
+                                fake + 16, nw, None) == -3
+    assert L.moe_backward_wgrad(ctypes.byref(layer), -1, fake, fake, fake, fake, nf, fake, nb, fake,
+                                nw, None) == -1
