@@ -138,38 +138,39 @@ __global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict_
     }
 }
 
-// Few tokens (T <= kSmallT): one warp per expert computes that expert's logit
-// for every token, streaming the centroid row once with all its loads in
-// flight.  Lane L holds columns 128 c + 4 L .. + 3 of every 128-column chunk c;
-// each 8-chunk run (32 products per lane and token) is a plain FMA chain,
-// added with TwoSum, and the lanes' sums are combined by a TwoSum butterfly
-// (every lane ends with the same value).  No split partials, no atomics.
+// Few tokens (T <= kSmallT): one block of four warps per expert computes that
+// expert's logit for every token, streaming the centroid row once with its
+// loads spread over the four warps.  Warp w takes the 128-column chunks
+// w, w + 4, ...; lane L holds columns 4 L .. 4 L + 3 of each chunk.  Each run
+// of up to eight of a warp's chunks (32 products per lane and token) is a plain
+// FMA chain, added with TwoSum; the lanes' sums are combined by a TwoSum
+// butterfly, and the four warps' sums in warp order by thread 0.  No split
+// partials, no atomics: the result does not depend on timing.
 constexpr int kSmallT = 8;
 __global__ void __launch_bounds__(128) logits_small_kernel(const uint16_t* __restrict__ u,
                                                            const float* __restrict__ c, int T,
                                                            int d, int E, float* __restrict__ l) {
-    const int e = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (e >= E) return;
+    __shared__ float wacc[4][kSmallT], wcmp[4][kSmallT];
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* crow = c + (size_t)e * d + lane * 4;
     float acc[kSmallT], cmp[kSmallT], chain[kSmallT];
 #pragma unroll
     for (int t = 0; t < kSmallT; ++t) acc[t] = cmp[t] = chain[t] = 0.0f;
     const int nch = d / 128;
-    for (int c0 = 0; c0 < nch; c0 += 8) {
-        const int n = min(8, nch - c0);
+    for (int c0 = warp; c0 < nch; c0 += 32) {           // eight of this warp's chunks per pass
         float4 cv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            if (i < n) cv[i] = *reinterpret_cast<const float4*>(crow + (size_t)(c0 + i) * 128);
+            if (c0 + 4 * i < nch) cv[i] = *reinterpret_cast<const float4*>(crow + (size_t)(c0 + 4 * i) * 128);
 #pragma unroll
         for (int t = 0; t < kSmallT; ++t) {
             if (t >= T) break;
             const uint16_t* ur = u + (size_t)t * d + lane * 4;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                if (i >= n) break;
-                const uint2 w = *reinterpret_cast<const uint2*>(ur + (size_t)(c0 + i) * 128);
+                if (c0 + 4 * i >= nch) break;
+                const uint2 w = *reinterpret_cast<const uint2*>(ur + (size_t)(c0 + 4 * i) * 128);
                 chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu)), cv[i].x, chain[t]);
                 chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16)), cv[i].y, chain[t]);
                 chain[t] = fmaf(bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu)), cv[i].z, chain[t]);
@@ -192,7 +193,22 @@ __global__ void __launch_bounds__(128) logits_small_kernel(const uint16_t* __res
             acc[t] = two_sum(acc[t], oa, err);
             cmp[t] = (cmp[t] + oc) + err;
         }
-        if (lane == 0) l[(size_t)t * E + e] = acc[t] + cmp[t];
+        if (lane == 0) {
+            wacc[warp][t] = acc[t];
+            wcmp[warp][t] = cmp[t];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        const int t = threadIdx.x;
+        float a = wacc[0][t], cm = wcmp[0][t];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+            float err;
+            a = two_sum(a, wacc[w][t], err);
+            cm = (cm + wcmp[w][t]) + err;
+        }
+        l[(size_t)t * E + e] = a + cm;
     }
 }
 
@@ -310,7 +326,7 @@ int launch_route(const uint16_t* u, const float* cent, const float* bias, int T,
     const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
     int split = 1;
     if (T <= kSmallT) {
-        logits_small_kernel<<<(E + 3) / 4, 128, 0, st>>>(u, cent, T, d, E, logits);
+        logits_small_kernel<<<E, 128, 0, st>>>(u, cent, T, d, E, logits);
         if ((rc = check_launch())) return rc;
         part = nullptr;
     } else {
