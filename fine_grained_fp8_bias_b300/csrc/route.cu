@@ -7,8 +7,10 @@
 // "Auxiliary-Loss-Free Load Balancing": the bias b_i only steers which
 // experts are chosen; the gate values use the unbiased s.
 //
-// Two kernels: a float32 GEMM for the logits l = u E^T on CUDA cores, then
-// one warp per token for sigmoid, selection and gates.  The logits feed a
+// Two kernels: the logits l = u E^T on CUDA cores (a tiled float32 GEMM, or
+// for at most kSmallT tokens one block per expert streaming its centroid
+// row), then one warp per token for sigmoid, selection and gates.  Used by
+// moe_route_noalloc and, below 256 tokens, by the layer.  The logits feed a
 // selection whose near-tie band is 1e-6 wide, so they are summed with
 // compensation: each 32-element chunk is a plain FMA chain, and the chunk
 // sums are added with TwoSum (Knuth's error-free addition), keeping the

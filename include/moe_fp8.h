@@ -255,7 +255,12 @@ int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
  * GEMM (down), combine -- all enqueued on `stream` with no host sync.
  * Outputs: h_out [T, d] float32 and the routing (topk_idx, topk_gate,
  * counts, tie_flag as in moe_route, or moe_route_grouped when L->n_groups >
- * 0), which moe_update_bias consumes.
+ * 0), which moe_update_bias consumes.  Below 256 tokens without group
+ * limits the logits are all summed exactly on CUDA cores (the router of
+ * moe_route_noalloc, with partial sums added in a fixed order) instead of
+ * the tensor-core screen: the same selection rule and tie flag; only tokens
+ * flagged as near ties may select differently from moe_route.  Repeated
+ * calls on the same input give identical results.
  * ws: at least moe_workspace_size(L, T) bytes, 256-byte aligned.  Its first
  * 16 bytes hold the device status word of this call (read it with
  * moe_check_device_status(ws, stream)). */
