@@ -60,6 +60,8 @@ int check_layer(const moe_layer_t* L) {
     if (!L) return MOE_ERR_INVALID_ARG;
     if (L->d <= 0 || L->E <= 0 || L->K <= 0 || L->S < 0 || L->I <= 0) return MOE_ERR_INVALID_ARG;
     if (L->E > kMaxExperts || L->K > kMaxTopK || L->K > L->E) return MOE_ERR_INVALID_ARG;
+    // the dispatch quantiser gives each of a token's K + S rows its own lane
+    if (L->K + L->S > 32) return MOE_ERR_INVALID_ARG;
     if (L->d % 128 || L->I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (L->E + L->S > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!L->centroids || !L->bias || !L->w_gate || !L->w_up || !L->w_down || !L->s_gate ||

@@ -374,10 +374,12 @@ int launch_route(const uint16_t* u, const float* cent, const float* bias, int T,
 // In host code the array's name is only a host-side stand-in, so its device
 // address is looked up with cudaGetSymbolAddress, once per device, with that
 // device current, on the first call made there.  Every call shares the
-// array and it keeps the last call's contents: the split-K path clears the
-// logits before it accumulates into them, and two calls that overlap on the
+// array and it keeps the last call's contents; two calls that overlap on the
 // GPU (different streams, or different host threads on one device) race on
-// it.
+// it.  The array's first T * E floats hold the logits and the rest holds the
+// split-K partial sums, as many splits as fit, which the selection kernel
+// adds in a fixed order: repeated calls on the same input give identical
+// results (no atomics; nothing read before it is written in the same call).
 namespace moe {
 namespace {
 
@@ -423,6 +425,8 @@ extern "C" int moe_route_noalloc(const uint16_t* u, const float* centroids, cons
     float* logits = nullptr;
     const int rc = noalloc_scratch(&logits);
     if (rc) return rc;
+    const size_t TE = (size_t)T * (size_t)E;
     return launch_route(u, centroids, bias, T, d, E, K, topk_idx, topk_gate, tie_flag, counts,
-                        logits, static_cast<cudaStream_t>(stream));
+                        logits, static_cast<cudaStream_t>(stream), logits + TE,
+                        kNoAllocMaxLogits - TE);
 }

@@ -36,17 +36,21 @@ class MoELayer:
 
     # ------------------------------------------------------------ set-up
     @classmethod
-    def from_config(cls, cfg: workloads.LayerConfig, device="cuda") -> "MoELayer":
+    def from_config(cls, cfg: workloads.LayerConfig, device="cuda", gen_device=None) -> "MoELayer":
         """Synthetic layer of a workload: seeded centroids, bias and master
-        weights, each weight matrix quantised 128x128 by moe_quant_128x128."""
+        weights, each weight matrix quantised 128x128 by moe_quant_128x128.
+        gen_device: where the generator draws the numbers (default: the
+        layer's device; "cpu" gives the same bits and launches no generator
+        kernels on the GPU, only the quantiser's)."""
         L = cls(cfg.d, cfg.E, cfg.K, cfg.S, cfg.I, device)
+        gdev = L.device if gen_device is None else torch.device(gen_device)
         L.set_group_routing(cfg.n_groups, cfg.topk_groups, cfg.group_topk)
-        L.centroids.copy_(workloads.centroids(cfg, L.device))
-        L.bias.copy_(workloads.bias(cfg, L.device))
+        L.centroids.copy_(workloads.centroids(cfg, gdev))
+        L.bias.copy_(workloads.bias(cfg, gdev))
         for g in range(L.G):
             for which, q, s in (("gate", L.w_gate, L.s_gate), ("up", L.w_up, L.s_up),
                                 ("down", L.w_down, L.s_down)):
-                w = workloads.master_weight(cfg, which, g, L.device)
+                w = workloads.master_weight(cfg, which, g, gdev).to(L.device)
                 lib.moe_quant_128x128(w, q[g], s[g])
         return L
 

@@ -142,6 +142,29 @@ def _bits(t: torch.Tensor, dtype) -> torch.Tensor:
     return t
 
 
+def _router_inputs(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor):
+    """Checks the router's inputs before their pointers reach a kernel:
+    u bf16 [T, d], centroids float32 [E, d] and bias float32 [E], all
+    contiguous on the same CUDA device.  Returns (T, d, E)."""
+    _bits(u, torch.bfloat16)
+    _bits(centroids, torch.float32)
+    _bits(bias, torch.float32)
+    for t, n in ((u, "u"), (centroids, "centroids"), (bias, "bias")):
+        _dev(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+        if t.device != u.device:
+            raise ValueError(f"{n} must be on {u.device}")
+    if u.dim() != 2 or centroids.dim() != 2 or bias.dim() != 1:
+        raise ValueError("need u [T, d], centroids [E, d], bias [E]")
+    T, d = u.shape
+    E = centroids.shape[0]
+    if centroids.shape[1] != d or bias.shape[0] != E:
+        raise ValueError(f"centroids {tuple(centroids.shape)} and bias {tuple(bias.shape)} "
+                         f"do not match u {tuple(u.shape)}")
+    return T, d, E
+
+
 def kernel_launches() -> int:
     return int(_lib.moe_kernel_launches())
 
@@ -208,10 +231,7 @@ def route_workspace_bytes(T: int, E: int, d: int) -> int:
 
 def moe_route(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, K: int,
               ws: Optional[torch.Tensor] = None, out: Optional[dict] = None, stream=None) -> dict:
-    _bits(u, torch.bfloat16)
-    _dev(u, "u")
-    T, d = u.shape
-    E = centroids.shape[0]
+    T, d, E = _router_inputs(u, centroids, bias)
     dev = u.device
     if out is None:
         out = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),
@@ -233,10 +253,7 @@ def moe_route_grouped(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tens
     """Group-limited routing: keep the topk_groups best of n_groups expert
     groups (score: sum of a group's group_topk best biased scores), then top-K
     inside them."""
-    _bits(u, torch.bfloat16)
-    _dev(u, "u")
-    T, d = u.shape
-    E = centroids.shape[0]
+    T, d, E = _router_inputs(u, centroids, bias)
     dev = u.device
     if out is None:
         out = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),
@@ -274,10 +291,7 @@ def moe_route_noalloc(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tens
     """moe_route without a workspace (the logits use the library's fixed
     device array; T * E <= 1048576; concurrent calls on one device race)."""
     fn = _lib.moe_route_noalloc
-    _bits(u, torch.bfloat16)
-    _dev(u, "u")
-    T, d = u.shape
-    E = centroids.shape[0]
+    T, d, E = _router_inputs(u, centroids, bias)
     dev = u.device
     if out is None:
         out = {"idx": torch.empty((T, K), dtype=torch.int32, device=dev),

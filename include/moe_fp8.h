@@ -62,7 +62,10 @@ enum moe_gemm_mode {
 
 /* One DeepSeekMoE layer: d hidden, E routed experts (top-K of them per
  * token), S shared experts, expert intermediate size I.  Weight stacks hold
- * the E routed experts first and the S shared experts after them. */
+ * the E routed experts first and the S shared experts after them.
+ * Limits checked by every call that takes a layer: 1 <= K <= min(E, 32),
+ * E <= 1024, E + S <= 1088, K + S <= 32 (a token has at most 32 dispatch
+ * rows), d and I multiples of 128. */
 typedef struct moe_layer_t {
     int d, E, K, S, I;
     const float* centroids;   /* [E, d] expert centroids e_i                          */
@@ -187,7 +190,9 @@ int moe_route_estimate_logits(const uint16_t* u, const float* centroids, int T, 
  * to float32 rounding: selections may differ only on flagged near-ties, gates
  * by a few ulps).  The [T, E] logits live in a
  * fixed 4 MB array in the library's device memory, so T * E must be at most
- * 1048576 (MOE_ERR_WORKSPACE otherwise).  The first call on each device looks
+ * 1048576 (MOE_ERR_WORKSPACE otherwise); the rest of the array holds split
+ * partial sums that are added in a fixed order, so repeated calls on the
+ * same input give identical results.  The first call on each device looks
  * up that array's device address (cudaGetSymbolAddress); make that first call
  * before any stream capture.  Every call shares the array: calls that
  * overlap on the GPU (other streams, other host threads) race on it.

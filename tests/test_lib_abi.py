@@ -158,3 +158,33 @@ def test_backward_entry_points_validate_on_the_host(lib):
                                 fake + 16, nw, None) == -3
     assert L.moe_backward_wgrad(ctypes.byref(layer), -1, fake, fake, fake, fake, nf, fake, nb, fake,
                                 nw, None) == -1
+
+
+def test_layer_with_more_than_32_rows_per_token_is_rejected(lib):
+    # K + S > 32: a token would need more dispatch rows than the quantiser's lanes
+    L = lib.lib()
+    fake = 1 << 20
+    layer = lib.moe_layer_t(256, 64, 32, 1, 128, *([fake] * 8))
+    assert L.moe_forward(ctypes.byref(layer), fake, 4, fake, fake, fake, fake, fake, fake,
+                         1 << 40, None) == -1
+    ok = lib.moe_layer_t(256, 64, 31, 1, 128, *([fake] * 8))
+    # K + S = 32 passes the layer checks (and then fails on the short workspace)
+    assert L.moe_forward(ctypes.byref(ok), fake, 4, fake, fake, fake, fake, fake, fake, 16,
+                         None) == -6
+
+
+def test_router_wrappers_check_their_inputs_on_the_host(lib):
+    # CPU tensors, wrong dtypes and mismatched shapes never reach a kernel
+    import torch
+    u = torch.zeros((4, 128), dtype=torch.bfloat16)
+    c = torch.zeros((8, 128), dtype=torch.float32)
+    b = torch.zeros((8,), dtype=torch.float32)
+    for fn in (lib.moe_route, lib.moe_route_noalloc):
+        with pytest.raises(ValueError):
+            fn(u, c, b, 2)                                   # host tensors
+        with pytest.raises(TypeError):
+            fn(u, c.half(), b, 2)                            # centroids not float32
+        with pytest.raises(TypeError):
+            fn(u.float(), c, b, 2)                           # u not bf16
+    with pytest.raises(ValueError):
+        lib._router_inputs(u, c, b)
