@@ -156,7 +156,8 @@ class Step:
         self.sa = torch.empty((d // 128, M), dtype=torch.float32, device=dev)
         self.H = torch.empty((M, I), dtype=torch.uint8, device=dev)
         self.sh = torch.empty((I // 128, M), dtype=torch.float32, device=dev)
-        self.Y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+        self.Y = torch.empty((T * K, d), dtype=torch.bfloat16, device=dev)
+        self.Ysh = torch.empty((T * S, d), dtype=torch.float32, device=dev)
         self.h = torch.empty((T, d), dtype=torch.float32, device=dev)
 
     def stage(self, name):
@@ -174,17 +175,19 @@ class Step:
             lib.moe_quant_1x128_dispatch(self.u, self.pout["inv_row"], L.K, L.S, q=self.A,
                                          scales=self.sa, status=self.status)
         elif name == "gemm_gate_up":
-            lib.moe_grouped_gemm_fp8(lib.MOE_GEMM_GATE_UP_SILU_QUANT, self.A, self.sa,
+            gemm = lib.moe_grouped_gemm_fp8_small if self.T <= 64 else lib.moe_grouped_gemm_fp8
+            gemm(lib.MOE_GEMM_GATE_UP_SILU_QUANT, self.A, self.sa,
                                      self.pout["group_offsets"], L.w_gate, L.w_up, L.s_gate,
                                      L.s_up, out=self.H, out_scales=self.sh, status=self.status)
         elif name == "gemm_down":
-            lib.moe_grouped_gemm_fp8(lib.MOE_GEMM_DOWN, self.H, self.sh,
-                                     self.pout["group_offsets"], L.w_down, None, L.s_down, None,
-                                     out=self.Y, status=self.status)
+            # routed rows bf16, shared rows float32; the small-group tiles for the
+            # gate/up GEMM up to 64 tokens and for the down GEMM up to 4 (as moe_forward)
+            lib.moe_grouped_gemm_fp8_down(self.H, self.sh, self.pout["group_offsets"], L.w_down,
+                                          L.s_down, L.E, self.T * L.K, self.Y, self.Ysh,
+                                          small_tiles=self.T <= 4, status=self.status)
         elif name == "combine":
-            TK = self.T * L.K
             lib.moe_combine(self.u, self.Y, self.rout["gate"], self.pout["inv_row"],
-                            self.Y[TK:] if L.S else None, L.S, h=self.h)
+                            self.Ysh if L.S else None, L.S, h=self.h)
         elif name == "bias_update":
             lib.moe_update_bias(self.rout["counts"], L.bias, self.T, L.K, self.gamma)
 
@@ -206,8 +209,10 @@ def algorithmic_bytes(cfg, T, touched: int) -> dict:
         "quant": T * d * 2 + M * 4 + M * d + M * (d // 128) * 4,
         "gemm_gate_up": touched * 2 * (I * d + wsc(I, d)) + M * d + M * (d // 128) * 4
         + M * I + M * (I // 128) * 4,
-        "gemm_down": touched * (d * I + wsc(d, I)) + M * I + M * (I // 128) * 4 + M * d * 2,
-        "combine": T * d * 2 + M * d * 2 + T * K * 8 + T * d * 4,
+        # expert outputs y: routed rows bf16, shared rows float32
+        "gemm_down": touched * (d * I + wsc(d, I)) + M * I + M * (I // 128) * 4
+        + T * K * d * 2 + T * S * d * 4,
+        "combine": T * d * 2 + T * K * d * 2 + T * S * d * 4 + T * K * 8 + T * d * 4,
         "bias_update": E * 4 * 3,
     }
 
@@ -235,6 +240,39 @@ def kernel_traffic(stage: str, workload: str):
     return e.get("dram_bytes_per_launch")
 
 
+def time_steps(step, steps):
+    """Times `steps` whole steps on the current stream with CUDA events: total
+    ms and the per-stage ms summed over the steps (an event after each stage)."""
+    stream = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in STAGES] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        step.run(evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    per_stage = {s: 0.0 for s in STAGES}
+    for k in range(steps):
+        for i, s in enumerate(STAGES):
+            a = start if (k == 0 and i == 0) else (evs[k][i - 1] if i > 0 else evs[k - 1][-1])
+            per_stage[s] += a.elapsed_time(evs[k][i])
+    return start.elapsed_time(stop), per_stage
+
+
+def kernel_table(cfg, T, touched, per_stage, steps):
+    abytes = algorithmic_bytes(cfg, T, touched)
+    flops = gemm_flops(cfg, T)
+    kernels = {}
+    for s in STAGES:
+        ms = per_stage[s] / steps
+        kernels[s] = {"ms": round(ms, 4), "share": round(per_stage[s] / sum(per_stage.values()), 4),
+                      "GBps": round(abytes[s] / (ms * 1e-3) / 1e9, 1)}
+        if s in flops:
+            kernels[s]["TFLOPs"] = round(flops[s] / (ms * 1e-3) / 1e12, 1)
+    return kernels, abytes, flops
+
+
 def run_ours(args, world, rank, local):
     from fine_grained_fp8_bias_b300 import lib
     from fine_grained_fp8_bias_b300.layer import MoELayer
@@ -246,7 +284,6 @@ def run_ours(args, world, rank, local):
     layer = MoELayer.from_config(cfg, dev)
     u = wl.tokens(cfg, dev)
     step = Step(layer, u, cfg.gamma)
-    stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
         step.run()
@@ -254,10 +291,6 @@ def run_ours(args, world, rank, local):
     if lib.moe_check_device_status(step.status) != 0:
         raise RuntimeError("device status flagged during warm-up")
 
-    n_ev = len(STAGES)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -265,21 +298,11 @@ def run_ours(args, world, rank, local):
     clocks.start()
     time.sleep(0.3)
     launches0 = lib.kernel_launches()
-    start.record(stream)
-    per_stage = {s: 0.0 for s in STAGES}
-    for k in range(args.steps):
-        step.run(evs[k])
-    stop.record(stream)
-    torch.cuda.synchronize()
+    total_ms, per_stage = time_steps(step, args.steps)
     launches = lib.kernel_launches() - launches0
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(stop)
-    for k in range(args.steps):
-        for i, s in enumerate(STAGES):
-            a = start if (k == 0 and i == 0) else (evs[k][i - 1] if i > 0 else evs[k - 1][-1])
-            per_stage[s] += a.elapsed_time(evs[k][i])
     if lib.moe_check_device_status(step.status) != 0:
         raise RuntimeError("device status flagged during the timed region")
 
@@ -291,32 +314,28 @@ def run_ours(args, world, rank, local):
     value = job_tokens_per_s(world, T, args.steps, total_ms)
 
     # per-kernel roofline
-    abytes = algorithmic_bytes(cfg, T, touched)
-    flops = gemm_flops(cfg, T)
-    kernels = {}
-    for s in STAGES:
-        ms = per_stage[s] / args.steps
-        kernels[s] = {"ms": round(ms, 4), "share": round(per_stage[s] / sum(per_stage.values()), 4),
-                      "GBps": round(abytes[s] / (ms * 1e-3) / 1e9, 1)}
-        if s in flops:
-            kernels[s]["TFLOPs"] = round(flops[s] / (ms * 1e-3) / 1e12, 1)
+    kernels, abytes, flops = kernel_table(cfg, T, touched, per_stage, args.steps)
     dom = max(STAGES, key=lambda s: per_stage[s])
     dom_ms = per_stage[dom] / args.steps
-    fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
-    # The dominant kernel runs inside a long loop of steps: its tensor peak is the
-    # sustained bf16 figure times the nominal FP8:BF16 ratio.  Above the ridge
-    # point (peak FLOP/s over copy bandwidth) it is bound by the tensor pipe.
-    fp8_sustained = (pk.get("bf16_tflops_sustained") or pk["bf16_tflops"]) * FP8_OVER_BF16
+    # FP8 dense peak: measured on this GPU (cuBLASLt e4m3 GEMM), burst for a kernel
+    # timed alone, sustained for a kernel timed inside a long loop of steps (the
+    # GEMMs here); without the probe, the bf16 figures x the nominal FP8:BF16 ratio.
+    fp8 = fp8_peak_probe(dev) if not args.no_fp8_probe else None
+    if fp8 and fp8.get("sustained_TFLOPs"):
+        fp8_sus, fp8_src = fp8["sustained_TFLOPs"], "measured e4m3 GEMM, sustained"
+    else:
+        fp8_sus = (pk.get("bf16_tflops_sustained") or pk["bf16_tflops"]) * FP8_OVER_BF16
+        fp8_src = f"{pk['source']} cuBLAS bf16 sustained x nominal FP8:BF16 ratio 2"
     intensity = flops.get(dom, 0.0) / abytes[dom]
-    ridge = fp8_sustained * 1e12 / (pk["hbm_gbs"] * 1e9)
+    ridge = fp8_sus * 1e12 / (pk["hbm_gbs"] * 1e9)
     if intensity > ridge:
         achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
-                    "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
-                    "frac": round(achieved / fp8_sustained, 4),
+                    "peak": round(fp8_sus, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / fp8_sus, 4),
                     "traffic": kernel_traffic(dom, cfg.name), "algorithmic_flops": flops[dom],
                     "algorithmic_bytes": abytes[dom], "flop_per_byte": round(intensity, 1),
-                    "peak_source": f"{pk['source']} cuBLAS bf16 sustained x nominal FP8:BF16 ratio 2"}
+                    "peak_source": fp8_src}
     else:
         achieved = abytes[dom] / (dom_ms * 1e-3) / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
@@ -324,16 +343,18 @@ def run_ours(args, world, rank, local):
                     "traffic": kernel_traffic(dom, cfg.name), "algorithmic_bytes": abytes[dom],
                     "flop_per_byte": round(intensity, 1),
                     "peak_source": f"{pk['source']} HBM copy bandwidth"}
-    fp8 = {s: {"TFLOPs": kernels[s]["TFLOPs"], "frac_of_fp8_peak": round(
-        kernels[s]["TFLOPs"] / fp8_peak, 4)} for s in flops}
-    fp8["peak_TFLOPs"] = fp8_peak
-    fp8["peak_source"] = f"{pk['source']} bf16 burst x nominal FP8/BF16 ratio 2"
+    fp8_gemm = {s: {"TFLOPs": kernels[s]["TFLOPs"],
+                    "frac_of_fp8_peak": round(kernels[s]["TFLOPs"] / fp8_sus, 4)} for s in flops}
+    fp8_gemm["peak_TFLOPs"] = round(fp8_sus, 1)
+    fp8_gemm["peak_source"] = fp8_src
 
     e2e = run_e2e(layer, cfg, dev, max(3, min(args.steps, 50)), world)
-    decode = run_decode(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
+    legs = args.workload == "v3_prefill" and not args.no_legs
+    decode = run_decode(layer, cfg, dev, pk) if legs else None
+    backward = run_backward(layer, cfg, dev, pk) if legs else None
+    wgrad = run_wgrad(layer, cfg, dev, pk) if legs else None
+    skew = run_skew(layer, dev, pk, fp8_sus) if legs else None
     balance = run_balance(layer, cfg, dev) if args.workload == "v3_long" else None
-    backward = run_backward(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
-    wgrad = run_wgrad(layer, cfg, dev, pk) if args.workload == "v3_prefill" else None
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -342,9 +363,11 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded counter-based generator; random-init weights quantised 128x128)",
         "config": {**wl.describe(cfg), "inputs": "resident in HBM; weights 11.3 GB > L2, no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roofline, "fp8_gemm": fp8, "kernels": kernels,
+        "roofline": roofline, "fp8_gemm": fp8_gemm, "kernels": kernels,
         "gpu_launches": launches, "clocks": clk, "e2e": e2e,
     }
+    if fp8:
+        line["fp8_peak_measured"] = fp8
     if decode:
         line["decode"] = decode
     if balance:
@@ -353,7 +376,130 @@ def run_ours(args, world, rank, local):
         line["backward_dgrad"] = backward
     if wgrad is not None:
         line["backward_wgrad"] = wgrad
+    if skew:
+        line["skew"] = skew
+    if legs:
+        # the tensor-bound configuration: its own layer (weights of its seed), after
+        # the prefill layer's memory is released
+        del step, layer
+        torch.cuda.empty_cache()
+        line["long"] = run_long(dev, pk, fp8_sus, fp8_src)
     return line
+
+
+def fp8_peak_probe(dev, n=8192, burst_reps=10, sustain_s=3.0):
+    """Dense FP8 (e4m3) tensor rate of this GPU: an n^3 GEMM through cuBLASLt
+    (torch._scaled_mm, bf16 output), best single call (burst) and back-to-back
+    calls for a few seconds (sustained, under the power cap), with the SM
+    clocks sampled meanwhile.  A measurement probe only: the layer never calls it."""
+    try:
+        g = torch.Generator(device=dev).manual_seed(7)
+        a = (torch.randn((n, n), device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
+        b = (torch.randn((n, n), device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        flop = 2.0 * n ** 3
+        best = float("inf")
+        for _ in range(burst_reps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            f()
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e))
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(10, int(sustain_s / (best * 1e-3)))
+        s.record()
+        for _ in range(reps):
+            f()
+        e.record()
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        ms = s.elapsed_time(e) / reps
+        del a, b
+        return {"burst_TFLOPs": round(flop / (best * 1e-3) / 1e12, 1),
+                "sustained_TFLOPs": round(flop / (ms * 1e-3) / 1e12, 1),
+                "shape": f"{n}x{n}x{n} e4m3 -> bf16", "sustained_calls": reps,
+                "clocks_sustained": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+                "how": "torch._scaled_mm (cuBLASLt), unit scales; best of "
+                       f"{burst_reps} (burst) and {reps} back-to-back calls (sustained)"}
+    except Exception as exc:                    # the probe is context; never fail the bench on it
+        return {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
+
+def run_skew(layer, dev, pk, fp8_sus, steps=50, warmup=5):
+    """The V3 prefill batch with skewed expert popularity (16 hot experts with
+    ~40% of the selections; the prefill weights, the skewed centroids): tokens/s
+    and the per-kernel breakdown."""
+    cfg = wl.V3_SKEW
+    saved_c, saved_b = layer.centroids.clone(), layer.bias.clone()
+    layer.centroids.copy_(wl.centroids(cfg, dev))
+    layer.bias.copy_(wl.bias(cfg, dev))
+    try:
+        step = Step(layer, wl.tokens(cfg, dev), cfg.gamma)
+        for _ in range(warmup):
+            step.run()
+        torch.cuda.synchronize()
+        total_ms, per_stage = time_steps(step, steps)
+        counts = step.rout["counts"].cpu()
+        from fine_grained_fp8_bias_b300 import lib
+        if lib.moe_check_device_status(step.status) != 0:
+            raise RuntimeError("device status flagged in the skew leg")
+    finally:
+        layer.centroids.copy_(saved_c)
+        layer.bias.copy_(saved_b)
+    touched = int((counts > 0).sum()) + cfg.S
+    kernels, abytes, _ = kernel_table(cfg, cfg.T, touched, per_stage, steps)
+    hot = float(counts[:cfg.hot_experts].sum()) / (cfg.T * cfg.K)
+    gu = kernels["gemm_gate_up"]
+    return {"workload": cfg.name, "steps": steps, "ms_per_step": round(total_ms / steps, 4),
+            "tokens_per_s": round(cfg.T * steps / (total_ms / 1e3), 1),
+            "hot_fraction": round(hot, 3), "max_expert_rows": int(counts.max()),
+            "gemm_gate_up_frac_of_hbm": round(gu["GBps"] / pk["hbm_gbs"], 4),
+            "kernels": kernels}
+
+
+def run_long(dev, pk, fp8_sus, fp8_src, steps=10, warmup=3):
+    """The tensor-bound configuration (T = 32768, V3 shapes, 4-component mixture
+    tokens, its own weights): tokens/s of the whole step, each GEMM's TFLOP/s as
+    a fraction of the measured FP8 peak, and the 100-step load-balancing run."""
+    from fine_grained_fp8_bias_b300 import lib
+    from fine_grained_fp8_bias_b300.layer import MoELayer
+    cfg = wl.V3_LONG
+    layer = MoELayer.from_config(cfg, dev)
+    step = Step(layer, wl.tokens(cfg, dev), cfg.gamma)
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    total_ms, per_stage = time_steps(step, steps)
+    clk = clocks.stop()
+    if lib.moe_check_device_status(step.status) != 0:
+        raise RuntimeError("device status flagged in the long leg")
+    counts = step.rout["counts"].cpu()
+    touched = int((counts > 0).sum()) + cfg.S
+    kernels, _, flops = kernel_table(cfg, cfg.T, touched, per_stage, steps)
+    out = {"workload": cfg.name, "T": cfg.T, "steps": steps,
+           "ms_per_step": round(total_ms / steps, 4),
+           "tokens_per_s": round(cfg.T * steps / (total_ms / 1e3), 1),
+           "fp8_peak_TFLOPs": round(fp8_sus, 1), "fp8_peak_source": fp8_src,
+           "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+           "kernels": kernels}
+    for s in flops:
+        out[s] = {"TFLOPs": kernels[s]["TFLOPs"],
+                  "frac_of_fp8_peak": round(kernels[s]["TFLOPs"] / fp8_sus, 4)}
+    del step
+    out["balance"] = run_balance(layer, cfg, dev)
+    del layer
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(layer, cfg, dev, steps, world):
@@ -597,6 +743,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v3_prefill", choices=sorted(wl.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="only the main workload (no decode, backward, skew, long legs)")
+    ap.add_argument("--no-fp8-probe", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -15,7 +15,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Workspace layout shared by moe_forward, moe_route and moe_permute.
 struct Layout {
-    size_t status, route, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, total;
+    size_t status, route, hist, base, go, offsets, perm, inv_row, A, sa, H, sh, Y, Ysh, total;
 };
 
 Layout layout(int T, int d, int E, int K, int S, int I) {
@@ -40,7 +40,9 @@ Layout layout(int T, int d, int E, int K, int S, int I) {
     L.sa = take(sizeof(float) * M * (d / 128));
     L.H = take(M * I);
     L.sh = take(sizeof(float) * M * (I / 128));
-    L.Y = take(sizeof(uint16_t) * M * d);
+    // routed expert outputs in bf16; the shared experts' (weight 1 in h') in float32
+    L.Y = take(sizeof(uint16_t) * (size_t)T * K * d);
+    L.Ysh = take(sizeof(float) * (size_t)T * S * d);
     L.total = off;
     return L;
 }
@@ -74,6 +76,22 @@ int check_layer(const moe_layer_t* L) {
 }
 
 inline cudaStream_t S_(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Batches of at most this many tokens run the gate/up GEMM, and of at most
+// kSmallDownT tokens the down GEMM, with the small-group tiles (measured on
+// B300 with the V3 decode shapes: gate/up 60 vs 74 us at T = 1, 888 vs 903 us
+// at T = 64; down equal at T = 1 to 4, slower with the small tiles from T = 16).
+constexpr int kSmallGemmT = 64;
+constexpr int kSmallDownT = 4;
+
+int launch_gemm_large(int mode, const uint8_t* A, const float* sa, int M_total, const int32_t* go,
+                      int G, const uint8_t* W0, const uint8_t* W1, const float* sw0,
+                      const float* sw1, int N, int Kdim, void* out, float* out_scales,
+                      int32_t* status, cudaStream_t st, int f32_group0, int f32_row0, float* out2) {
+    return launch_grouped_gemm(mode, A, sa, M_total, go, G, W0, W1, sw0, sw1, N, Kdim, out,
+                               out_scales, status, st, nullptr, f32_group0, f32_row0, out2);
+}
+
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -239,7 +257,8 @@ int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_tota
                          const int32_t* group_offsets, int G, const uint8_t* W0,
                          const uint8_t* W1, const float* sw0, const float* sw1, int N, int Kdim,
                          void* out, float* out_scales, int32_t* status, void* stream) {
-    if (mode != MOE_GEMM_GATE_UP_SILU_QUANT && mode != MOE_GEMM_DOWN) return MOE_ERR_INVALID_ARG;
+    if (mode != MOE_GEMM_GATE_UP_SILU_QUANT && mode != MOE_GEMM_DOWN && mode != MOE_GEMM_DOWN_F32)
+        return MOE_ERR_INVALID_ARG;
     if (M_total < 0 || G < 0 || N <= 0 || Kdim <= 0) return MOE_ERR_INVALID_ARG;
     if (N % 128 || Kdim % 128 || G > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)G * N > 0x7fffffffLL || (long long)M_total * (N > Kdim ? N : Kdim) > (1LL << 40))
@@ -254,8 +273,47 @@ int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_tota
                                out, out_scales, status, S_(stream));
 }
 
+int moe_grouped_gemm_fp8_small(int mode, const uint8_t* A, const float* sa, int M_total,
+                               const int32_t* group_offsets, int G, const uint8_t* W0,
+                               const uint8_t* W1, const float* sw0, const float* sw1, int N,
+                               int Kdim, void* out, float* out_scales, int32_t* status,
+                               void* stream) {
+    if (mode != MOE_GEMM_GATE_UP_SILU_QUANT && mode != MOE_GEMM_DOWN && mode != MOE_GEMM_DOWN_F32)
+        return MOE_ERR_INVALID_ARG;
+    if (M_total < 0 || G < 0 || N <= 0 || Kdim <= 0) return MOE_ERR_INVALID_ARG;
+    if (N % 128 || Kdim % 128 || G > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)G * N > 0x7fffffffLL || (long long)M_total * (N > Kdim ? N : Kdim) > (1LL << 40))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (M_total == 0 || G == 0) return MOE_OK;
+    if (!A || !sa || !group_offsets || !W0 || !sw0 || !out) return MOE_ERR_INVALID_ARG;
+    const bool gu = mode == MOE_GEMM_GATE_UP_SILU_QUANT;
+    if (gu && (!W1 || !sw1 || !out_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(W0) || (gu && !aligned16(W1)) || !aligned16(out))
+        return MOE_ERR_MISALIGNED;
+    return launch_grouped_gemm_small(mode, A, sa, M_total, group_offsets, G, W0, W1, sw0, sw1, N,
+                                     Kdim, out, out_scales, status, S_(stream));
+}
+
+int moe_grouped_gemm_fp8_down(const uint8_t* H, const float* sh, int M_total,
+                              const int32_t* group_offsets, int G, int f32_group0, int f32_row0,
+                              const uint8_t* W, const float* sw, int N, int Kdim, uint16_t* y,
+                              float* y_f32, int small_tiles, int32_t* status, void* stream) {
+    if (M_total < 0 || G < 0 || N <= 0 || Kdim <= 0 || f32_group0 < 0 || f32_row0 < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (N % 128 || Kdim % 128 || G > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)G * N > 0x7fffffffLL || (long long)M_total * (N > Kdim ? N : Kdim) > (1LL << 40))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (M_total == 0 || G == 0) return MOE_OK;
+    if (!H || !sh || !group_offsets || !W || !sw) return MOE_ERR_INVALID_ARG;
+    if ((f32_group0 > 0 && !y) || (f32_group0 < G && !y_f32)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(H) || !aligned16(W) || !aligned16(y) || !aligned16(y_f32)) return MOE_ERR_MISALIGNED;
+    const auto gemm = small_tiles ? launch_grouped_gemm_small : launch_gemm_large;
+    return gemm(MOE_GEMM_DOWN, H, sh, M_total, group_offsets, G, W, nullptr, sw, nullptr, N, Kdim,
+                y, nullptr, status, S_(stream), f32_group0, f32_row0, y_f32);
+}
+
 int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
-                const int32_t* inv_row, const uint16_t* Y_shared, int T, int d, int K, int S,
+                const int32_t* inv_row, const float* Y_shared, int T, int d, int K, int S,
                 float* h_out, void* stream) {
     if (T < 0 || d <= 0 || K < 0 || K > kMaxTopK || S < 0) return MOE_ERR_INVALID_ARG;
     if (d % 8) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -302,6 +360,7 @@ int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, i
     uint8_t* H = reinterpret_cast<uint8_t*>(base + W.H);
     float* sh = reinterpret_cast<float*>(base + W.sh);
     uint16_t* Y = reinterpret_cast<uint16_t*>(base + W.Y);
+    float* Ysh = reinterpret_cast<float*>(base + W.Ysh);
     const int M = T * (K + S);
 
     if (reset_status) {
@@ -317,13 +376,20 @@ int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, i
                              st)))
         return rc;
     if ((rc = launch_quant_dispatch(u, T, d, inv_row, K, S, A, sa, M, status, st))) return rc;
-    if ((rc = launch_grouped_gemm(MOE_GEMM_GATE_UP_SILU_QUANT, A, sa, M, go, G, L->w_gate,
-                                  L->w_up, L->s_gate, L->s_up, I, d, H, sh, status, st)))
+    // Few tokens: no group has more than T rows, so the weight panels dominate
+    // the bytes and the tiles of 128 weight rows x 32 rows keep more of them in
+    // flight per SM (gemm_small.cu).  Routed rows of y in bf16, shared rows
+    // (weight 1 in h') in float32.
+    const auto gemm = T <= kSmallGemmT ? launch_grouped_gemm_small : launch_gemm_large;
+    const auto gemm_down = T <= kSmallDownT ? launch_grouped_gemm_small : launch_gemm_large;
+    if ((rc = gemm(MOE_GEMM_GATE_UP_SILU_QUANT, A, sa, M, go, G, L->w_gate, L->w_up, L->s_gate,
+                   L->s_up, I, d, H, sh, status, st, 1 << 30, 0, nullptr)))
         return rc;
-    if ((rc = launch_grouped_gemm(MOE_GEMM_DOWN, H, sh, M, go, G, L->w_down, nullptr, L->s_down,
-                                  nullptr, d, I, Y, nullptr, status, st)))
+    // routed groups' rows (the first T*K) to Y in bf16, shared groups' rows to Ysh in float32
+    if ((rc = gemm_down(MOE_GEMM_DOWN, H, sh, M, go, G, L->w_down, nullptr, L->s_down, nullptr, d,
+                        I, Y, nullptr, status, st, E, T * K, Ysh)))
         return rc;
-    return launch_combine(u, Y, topk_gate, inv_row, Y + (size_t)T * K * d, T, d, K, S, h_out, st);
+    return launch_combine(u, Y, topk_gate, inv_row, Ysh, T, d, K, S, h_out, st);
 }
 
 // Backward workspace: status, dy codes and scales, dH, [dG | dU] codes and

@@ -95,13 +95,27 @@ int launch_wgrad_gemm(const uint8_t* At, const float* sAt, int Na, const uint8_t
 int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, int32_t* perm,
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);
+// DOWN modes: with out2 set, the rows of groups >= f32_group0 are stored as
+// float32 in out2 (row - f32_row0) and the other rows as bf16 in out.
 int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
                         const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                         const float* sw0, const float* sw1, int N, int Kdim, void* out,
                         float* out_scales, int32_t* status, cudaStream_t st,
-                        const uint16_t* dH = nullptr);
+                        const uint16_t* dH = nullptr, int f32_group0 = 1 << 30, int f32_row0 = 0,
+                        float* out2 = nullptr);
+// The same GEMM with tiles of 128 weight rows x up to 32 rows of a group
+// (gemm_small.cu; GATE_UP_SILU_QUANT and DOWN modes): for groups with few rows.
+int launch_grouped_gemm_small(int mode, const uint8_t* A, const float* sa, int M_total,
+                              const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
+                              const float* sw0, const float* sw1, int N, int Kdim, void* out,
+                              float* out_scales, int32_t* status, cudaStream_t st,
+                              int f32_group0 = 1 << 30, int f32_row0 = 0, float* out2 = nullptr);
+// The combine: routed rows Y bf16 with shared rows Ysh float32 (the forward),
+// or both bf16 (the input gradient's rows, gathered with gate = NULL).
 int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
                    const uint16_t* Ysh, int T, int d, int K, int S, float* h, cudaStream_t st);
+int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
+                   const float* Ysh, int T, int d, int K, int S, float* h, cudaStream_t st);
 int launch_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,
                        cudaStream_t st);
 

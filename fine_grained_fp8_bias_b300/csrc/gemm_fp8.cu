@@ -116,6 +116,11 @@ struct Params {
     int32_t* status;
     int* counter;                               // next unclaimed tile (nullable: static order)
     const uint16_t* dH;                         // gradient of h [M_total, N] bf16 (gradient mode)
+    // DOWN: rows of groups >= f32_group0 go to out2 (float32, row - f32_row0);
+    // the others to out (bf16)
+    int f32_group0;
+    int f32_row0;
+    float* out2;
 };
 
 // ----------------------------------------------------------- tile lookup
@@ -608,6 +613,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             p.out_scales[(size_t)(half * NB + tl.nt) * p.M_total + grow] = scale;
                     }
                 }
+            } else if (valid && cols_valid && tl.g >= p.f32_group0) {
+                float* dst = p.out2 + (size_t)(grow - p.f32_row0) * p.N + tl.nt * BN + wg * 128;
+#pragma unroll
+                for (int j = 0; j < 128; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
             } else if (valid && cols_valid) {
                 uint16_t* dst = static_cast<uint16_t*>(p.out) + (size_t)grow * p.N + tl.nt * BN + wg * 128;
 #pragma unroll
@@ -639,7 +649,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
                         const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                         const float* sw0, const float* sw1, int N, int Kdim, void* out,
-                        float* out_scales, int32_t* status, cudaStream_t st, const uint16_t* dH) {
+                        float* out_scales, int32_t* status, cudaStream_t st, const uint16_t* dH,
+                        int f32_group0, int f32_row0, float* out2) {
     if (M_total == 0 || G == 0) return MOE_OK;
     static int sm_count = 0;
     static std::once_flag once;
@@ -666,7 +677,8 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
     if (sm_count <= 0) return cuda_fail(cudaErrorInvalidDevice);
     // The warpgroups re-split the registers the CTA is launched with; launching
     // with fewer than LAUNCH_REGS per thread would leave setmaxnreg.inc waiting.
-    const int kmode = mode == MOE_GEMM_DOWN ? 0 : (mode == MOE_GEMM_GATE_UP_SILU_QUANT ? 1 : 2);
+    const bool down = mode == MOE_GEMM_DOWN || mode == MOE_GEMM_DOWN_F32;
+    const int kmode = down ? 0 : (mode == MOE_GEMM_GATE_UP_SILU_QUANT ? 1 : 2);
     const bool gu = kmode != 0;
     if (num_regs[kmode] != LAUNCH_REGS) return cuda_fail(cudaErrorInvalidConfiguration);
     CUtensorMap mA, mB0, mB1;
@@ -687,7 +699,13 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
         const cudaError_t ce = cudaMemsetAsync(counter, 0, sizeof(int), st);
         if (ce != cudaSuccess) return cuda_fail(ce);
     }
-    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter, dH};
+    if (mode == MOE_GEMM_DOWN_F32) {                // every group's rows in float32
+        f32_group0 = 0;
+        f32_row0 = 0;
+        out2 = static_cast<float*>(out);
+    }
+    Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter, dH,
+             down && out2 ? f32_group0 : (1 << 30), f32_row0, out2};
     const int NT = gu ? N / 128 : (N + BN - 1) / BN;
     const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NT;
     const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);

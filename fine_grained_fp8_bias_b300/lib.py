@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libmoefp8.so")
 MOE_OK = 0
 MOE_GEMM_GATE_UP_SILU_QUANT = 1
 MOE_GEMM_DOWN = 2
+MOE_GEMM_DOWN_F32 = 4
 
 P = ctypes.c_void_p
 I32 = ctypes.c_int
@@ -82,6 +83,8 @@ def _load() -> ctypes.CDLL:
         "moe_route_estimate_logits": [P, P, I32, I32, I32, P, P, P, ctypes.c_size_t, P],
         "moe_permute": [P, I32, I32, I32, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_grouped_gemm_fp8": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
+        "moe_grouped_gemm_fp8_small": [I32, P, P, I32, P, I32, P, P, P, P, I32, I32, P, P, P, P],
+        "moe_grouped_gemm_fp8_down": [P, P, I32, P, I32, I32, I32, P, P, I32, I32, P, P, I32, P, P],
         "moe_combine": [P, P, P, P, P, I32, I32, I32, I32, P, P],
         "moe_forward": [ctypes.POINTER(moe_layer_t), P, I32, P, P, P, P, P, P, ctypes.c_size_t, P],
         "moe_update_bias": [P, I32, I32, I32, ctypes.c_float, P, P],
@@ -326,6 +329,11 @@ def moe_permute(topk_idx: torch.Tensor, E: int, S: int = 0, ws: Optional[torch.T
     return out
 
 
+def _out_dtype(mode: int):
+    return {MOE_GEMM_GATE_UP_SILU_QUANT: torch.uint8, MOE_GEMM_DOWN_F32: torch.float32}.get(
+        mode, torch.bfloat16)
+
+
 def moe_grouped_gemm_fp8(mode: int, A: torch.Tensor, sa: torch.Tensor,
                          group_offsets: torch.Tensor, W0: torch.Tensor,
                          W1: Optional[torch.Tensor], sw0: torch.Tensor,
@@ -338,8 +346,7 @@ def moe_grouped_gemm_fp8(mode: int, A: torch.Tensor, sa: torch.Tensor,
     G, N, _ = W0.shape
     dev = A.device
     if out is None:
-        out = torch.empty((M_total, N), dtype=torch.uint8 if mode == MOE_GEMM_GATE_UP_SILU_QUANT
-                          else torch.bfloat16, device=dev)
+        out = torch.empty((M_total, N), dtype=_out_dtype(mode), device=dev)
     if mode == MOE_GEMM_GATE_UP_SILU_QUANT and out_scales is None:
         out_scales = torch.empty((N // 128, M_total), dtype=torch.float32, device=dev)
     _check(_lib.moe_grouped_gemm_fp8(mode, _ptr(A), _ptr(sa), M_total, _ptr(group_offsets), G,
@@ -349,9 +356,58 @@ def moe_grouped_gemm_fp8(mode: int, A: torch.Tensor, sa: torch.Tensor,
     return (out, out_scales) if mode == MOE_GEMM_GATE_UP_SILU_QUANT else out
 
 
+def moe_grouped_gemm_fp8_small(mode: int, A: torch.Tensor, sa: torch.Tensor,
+                               group_offsets: torch.Tensor, W0: torch.Tensor,
+                               W1: Optional[torch.Tensor], sw0: torch.Tensor,
+                               sw1: Optional[torch.Tensor], out: Optional[torch.Tensor] = None,
+                               out_scales: Optional[torch.Tensor] = None,
+                               status: Optional[torch.Tensor] = None, stream=None):
+    """moe_grouped_gemm_fp8 with the small-group tiles (same arguments and results)."""
+    _dev(A, "A")
+    M_total, Kdim = A.shape
+    G, N, _ = W0.shape
+    dev = A.device
+    if out is None:
+        out = torch.empty((M_total, N), dtype=_out_dtype(mode), device=dev)
+    if mode == MOE_GEMM_GATE_UP_SILU_QUANT and out_scales is None:
+        out_scales = torch.empty((N // 128, M_total), dtype=torch.float32, device=dev)
+    _check(_lib.moe_grouped_gemm_fp8_small(mode, _ptr(A), _ptr(sa), M_total, _ptr(group_offsets),
+                                           G, _ptr(W0), _ptr(W1), _ptr(sw0), _ptr(sw1), N, Kdim,
+                                           _ptr(out), _ptr(out_scales), _ptr(status),
+                                           _stream(stream)), "moe_grouped_gemm_fp8_small")
+    return (out, out_scales) if mode == MOE_GEMM_GATE_UP_SILU_QUANT else out
+
+
+def moe_grouped_gemm_fp8_down(H: torch.Tensor, sh: torch.Tensor, group_offsets: torch.Tensor,
+                              W: torch.Tensor, sw: torch.Tensor, f32_group0: int, f32_row0: int,
+                              y: Optional[torch.Tensor], y_f32: Optional[torch.Tensor],
+                              small_tiles: bool = False, status: Optional[torch.Tensor] = None,
+                              stream=None):
+    """The layer's down projection: rows of groups < f32_group0 to y (bf16),
+    rows of the later groups to y_f32 (float32, row - f32_row0)."""
+    _dev(H, "H")
+    M_total, Kdim = H.shape
+    G, N, _ = W.shape
+    if y is not None:
+        _bits(y, torch.bfloat16)
+    if y_f32 is not None:
+        _bits(y_f32, torch.float32)
+    _check(_lib.moe_grouped_gemm_fp8_down(_ptr(H), _ptr(sh), M_total, _ptr(group_offsets), G,
+                                          f32_group0, f32_row0, _ptr(W), _ptr(sw), N, Kdim, _ptr(y),
+                                          _ptr(y_f32), 1 if small_tiles else 0, _ptr(status),
+                                          _stream(stream)), "moe_grouped_gemm_fp8_down")
+    return y, y_f32
+
+
 def moe_combine(u: torch.Tensor, Y: torch.Tensor, topk_gate: torch.Tensor, inv_row: torch.Tensor,
                 Y_shared: Optional[torch.Tensor], S: int, h: Optional[torch.Tensor] = None,
                 stream=None) -> torch.Tensor:
+    """h' = u + shared rows + gate-weighted routed rows; Y bf16 (routed rows),
+    Y_shared float32 (the outputs of moe_grouped_gemm_fp8_down)."""
+    _bits(u, torch.bfloat16)
+    _bits(Y, torch.bfloat16)
+    if Y_shared is not None:
+        _bits(Y_shared, torch.float32)
     T, d = u.shape
     K = topk_gate.shape[1]
     if h is None:

@@ -57,7 +57,8 @@ enum moe_status {
 enum moe_gemm_mode {
     MOE_GEMM_GATE_UP_SILU_QUANT = 1, /* h = SiLU(A W_gate^T) * (A W_up^T), re-quantised 1x128 */
     MOE_GEMM_DOWN = 2,               /* y = A W_down^T, stored as bf16                         */
-    MOE_GEMM_GATE_UP_DGRAD = 3       /* [dG | dU] from recomputed G, U and dH (moe_backward_dgrad) */
+    MOE_GEMM_GATE_UP_DGRAD = 3,      /* [dG | dU] from recomputed G, U and dH (moe_backward_dgrad) */
+    MOE_GEMM_DOWN_F32 = 4            /* y = A W_down^T, stored as float32                      */
 };
 
 /* One DeepSeekMoE layer: d hidden, E routed experts (top-K of them per
@@ -234,6 +235,7 @@ int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* of
  *     per 1x128 tile with the moe_quant_1x128 rule.
  *   mode DOWN: W0 = W_down, N = d; out = y [M_total, N] bf16 (round to
  *     nearest even); out_scales unused.
+ *   mode DOWN_F32: as DOWN with y stored as float32.
  * Rows outside every group are left untouched.  Kdim and N multiples of 128;
  * G <= 1088; all pointers 16-byte aligned.  status (device int32 [2],
  * nullable): status[0] receives MOE_ERR_TIMEOUT if a pipeline wait ran out
@@ -246,14 +248,45 @@ int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_tota
                          const uint8_t* W1, const float* sw0, const float* sw1, int N, int Kdim,
                          void* out, float* out_scales, int32_t* status, void* stream);
 
+/* moe_grouped_gemm_fp8 for groups with few rows (decode batches; modes
+ * GATE_UP_SILU_QUANT and DOWN): same arguments, arithmetic and results, with
+ * tiles of 128 weight rows by up to 32 rows of a group (the weight block on
+ * the tensor core's M side, the rows on its N side).  A group's rows are cut
+ * into chunks of 32, each a tile of its own, so a group with many rows (a hot
+ * expert) is spread over as many CTAs; the chunks of one weight panel are
+ * claimed together and read the panel from HBM once.  moe_forward uses it
+ * for the gate/up GEMM of batches of at most 64 tokens and for the down
+ * GEMM of batches of at most 4. */
+int moe_grouped_gemm_fp8_small(int mode, const uint8_t* A, const float* sa, int M_total,
+                               const int32_t* group_offsets, int G, const uint8_t* W0,
+                               const uint8_t* W1, const float* sw0, const float* sw1, int N,
+                               int Kdim, void* out, float* out_scales, int32_t* status,
+                               void* stream);
+
+/* The layer's down projection (moe_grouped_gemm_fp8 in DOWN mode, same
+ * arithmetic) with its outputs split by precision: the rows of groups
+ * [0, f32_group0) go to y [*, N] as bf16, the rows of groups
+ * [f32_group0, G) to y_f32 [*, N] as float32 at row (row - f32_row0).  The
+ * layer passes f32_group0 = E and f32_row0 = T*K: routed outputs in bf16,
+ * shared outputs (rows T*K ...) in float32.  small_tiles != 0 selects the
+ * tiles of moe_grouped_gemm_fp8_small.  H [M_total, Kdim] fp8 with sh
+ * [Kdim/128][M_total]; W [G, N, Kdim] fp8 with sw [G, N/128, Kdim/128];
+ * status as in moe_grouped_gemm_fp8. */
+int moe_grouped_gemm_fp8_down(const uint8_t* H, const float* sh, int M_total,
+                              const int32_t* group_offsets, int G, int f32_group0, int f32_row0,
+                              const uint8_t* W, const float* sw, int N, int Kdim, uint16_t* y,
+                              float* y_f32, int small_tiles, int32_t* status, void* stream);
+
 /* Combine ([TH] Method §2: h'_t = u_t + sum_s FFN_s(u_t) + sum_i g_{i,t}
  * FFN_i(u_t)).  h_out[t] = u[t] + sum_s Y_shared[s*T + t] +
  * sum_k topk_gate[t,k] * Y[inv_row[t,k]], summed in float32.
- *   u [T, d] bf16; Y [*, d] bf16 (routed rows); Y_shared [S*T, d] bf16
- *   (may be NULL when S = 0); h_out [T, d] float32.  d multiple of 8;
- *   pointers 16-byte aligned. */
+ *   u [T, d] bf16; Y [*, d] bf16 (routed rows); Y_shared [S*T, d] float32
+ *   (the shared experts' outputs, which enter h' with weight 1, are kept in
+ *   float32; the bf16 rounding of the routed outputs is averaged by gates
+ *   that sum to 1; may be NULL when S = 0); h_out [T, d] float32 (the rows of
+ *   moe_grouped_gemm_fp8_down).  d multiple of 8; pointers 16-byte aligned. */
 int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
-                const int32_t* inv_row, const uint16_t* Y_shared, int T, int d, int K, int S,
+                const int32_t* inv_row, const float* Y_shared, int T, int d, int K, int S,
                 float* h_out, void* stream);
 
 /* The whole layer forward: route, dispatch, quantise, GEMM (gate/up + SiLU),

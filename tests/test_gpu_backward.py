@@ -60,7 +60,7 @@ def _check(orc, cfg, tokens=None):
     u_cpu = u.cpu()
     r = orc.route(bits(u_cpu), wl.centroids(cfg).numpy(), wl.bias(cfg).numpy(), cfg.K)
     gidx, ggate = out["idx"].cpu().numpy(), out["gate"].cpu().numpy()
-    bad = routing_agreement(gidx, ggate, r)
+    bad = routing_agreement(gidx, ggate, r, bias=wl.bias(cfg).numpy())
     toks = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
     toks = np.array([t for t in toks if t not in set(bad.tolist())], np.int64)
     need = set(range(cfg.E, cfg.E + cfg.S)) | {int(e) for t in toks for e in gidx[t]}

@@ -4,38 +4,47 @@ import pytest
 import torch
 
 from fine_grained_fp8_bias_b300 import workloads as wl
-from tests.helpers import MAX_ABS, REL_FRO, bits, oracle_weights, rel_fro, routing_agreement
+from tests.helpers import (MAX_ABS, REL_FRO, bits, layer_forward_threaded, oracle_weights_threaded,
+                           rel_fro, route_threaded, routing_agreement, tile_covering_tokens)
 
 pytestmark = pytest.mark.gpu
 
 
-def gpu_forward(cfg, step=0, layer=None):
+def gpu_forward(cfg, step=0, layer=None, u=None):
     from fine_grained_fp8_bias_b300.layer import MoELayer
     L = layer or MoELayer.from_config(cfg, "cuda")
-    u = wl.tokens(cfg, "cuda", step)
+    u = wl.tokens(cfg, "cuda", step) if u is None else u
     out = L.forward(u)
     torch.cuda.synchronize()
     assert L.status() == 0
     return L, u, out
 
 
-def check_layer(orc, cfg, tokens=None, layer=None):
-    L, u, out = gpu_forward(cfg, layer=layer)
+def check_layer(orc, cfg, tokens=None, layer=None, u=None, cover=(64, 256)):
+    """Layer output of the CUDA path against the oracle on the listed tokens
+    (all tokens when None; "cover": tokens whose dispatch rows reach every
+    shared-expert M tile and the first, last and last-tile rows of cover[0]
+    routed experts, cover[1] tokens in all)."""
+    L, u, out = gpu_forward(cfg, layer=layer, u=u)
     u_cpu = u.cpu()
-    r = orc.route(bits(u_cpu), wl.centroids(cfg).numpy(), wl.bias(cfg).numpy(), cfg.K)
+    r = route_threaded(orc, bits(u_cpu), wl.centroids(cfg).numpy(), wl.bias(cfg).numpy(), cfg.K)
     gidx = out["idx"].cpu().numpy()
-    bad = routing_agreement(gidx, out["gate"].cpu().numpy(), r)
-    toks = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
+    bad = routing_agreement(gidx, out["gate"].cpu().numpy(), r, bias=wl.bias(cfg).numpy())
+    if isinstance(tokens, str) and tokens == "cover":
+        toks, picked = tile_covering_tokens(r["idx"], cfg, n_groups=cover[0], total=cover[1])
+    else:
+        toks, picked = (np.arange(cfg.T) if tokens is None else np.asarray(tokens)), []
     toks = np.array([t for t in toks if t not in set(bad.tolist())], np.int64)
     need = set(range(cfg.E, cfg.E + cfg.S))
     for t in toks:
         need.update(int(e) for e in r["idx"][t])
-    W = oracle_weights(orc, cfg, need)
-    ref = orc.layer_forward(bits(u_cpu), r["idx"], r["gate"], W, cfg.d, cfg.E, cfg.K, cfg.S, cfg.I, toks)
+    W = oracle_weights_threaded(orc, cfg, need)
+    ref = layer_forward_threaded(orc, bits(u_cpu), r["idx"], r["gate"], W, cfg, toks)
     got = out["h"].cpu().numpy()[toks]
     err_f, err_m = rel_fro(got, ref), float(np.abs(got - ref).max())
-    print(f"{cfg.name}: tokens {len(toks)} rel_fro {err_f:.3e} max_abs {err_m:.3e} "
-          f"flagged {int(r['tie'].sum())} mismatched {len(bad)}")
+    print(f"{cfg.name}: tokens {len(toks)} (experts {len(need)}, covered groups {len(picked)}) "
+          f"rel_fro {err_f:.3e} max_abs {err_m:.3e} flagged {int(r['tie'].sum())} "
+          f"mismatched {len(bad)}")
     assert err_f <= REL_FRO and err_m <= MAX_ABS
     # the routed part alone (h' - u) must also be close: u does not hide errors
     du = u_cpu.float().numpy()[toks]
@@ -64,9 +73,60 @@ def test_mid_sampled(orc):
     check_layer(orc, wl.MID, tokens=[0, 1, 777, 2048, 4095])
 
 
-def test_v3_prefill_sampled(orc):
-    # the benchmark's workload and launch configuration, checked on sampled tokens
-    check_layer(orc, wl.V3_PREFILL, tokens=[0, 4095])
+@pytest.fixture(scope="module")
+def v3_layer():
+    # V3 prefill and its skewed form share the weight seed: one device copy
+    from fine_grained_fp8_bias_b300.layer import MoELayer
+    L = MoELayer.from_config(wl.V3_PREFILL, "cuda")
+    yield L
+    del L
+    torch.cuda.empty_cache()
+
+
+def test_v3_prefill_sampled(orc, v3_layer):
+    # the benchmark's workload and launch configuration, checked on >= 256 tokens
+    # whose rows cover all 32 M tiles of the shared expert and the first, last and
+    # ragged-last-tile rows of 64 routed experts plus the largest and smallest
+    check_layer(orc, wl.V3_PREFILL, tokens="cover", layer=v3_layer)
+
+
+def test_v3_skew_sampled(orc, v3_layer):
+    # 16 hot experts take ~40% of the selections: their groups span many M tiles
+    cfg = wl.V3_SKEW
+    v3_layer.centroids.copy_(wl.centroids(cfg, "cuda"))
+    try:
+        _, _, out, r = check_layer(orc, cfg, tokens="cover", layer=v3_layer, cover=(64, 256))
+        hot = r["counts"][:cfg.hot_experts].sum() / (cfg.T * cfg.K)
+        assert hot > 0.3, hot
+    finally:
+        v3_layer.centroids.copy_(wl.centroids(wl.V3_PREFILL, "cuda"))
+
+
+def with_outliers(cfg, u, n_tok=48, scale=100.0):
+    """u with one isolated large activation (+-scale, i.e. >= 100 sigma of the
+    N(0, 1) draw) in one 1x128 tile of each of n_tok tokens: the case 1x128
+    tile scaling is for (the outlier sets only its own tile's scale)."""
+    u = u.clone()
+    rng = np.random.default_rng(cfg.seed + 1000)
+    toks = rng.choice(cfg.T, size=min(n_tok, cfg.T), replace=False)
+    cols = rng.integers(0, cfg.d, size=len(toks))
+    sign = rng.choice([-1.0, 1.0], size=len(toks))
+    for t, c, sg in zip(toks, cols, sign):
+        u[int(t), int(c)] = float(sg * scale)
+    return u, np.sort(toks)
+
+
+def test_mid_outliers(orc):
+    cfg = wl.MID
+    u, toks = with_outliers(cfg, wl.tokens(cfg, "cuda"), n_tok=48)
+    # every token with an outlier, plus a few without
+    check_layer(orc, cfg, tokens=list(toks) + [0, 1, cfg.T - 1], u=u)
+
+
+def test_v3_prefill_outliers(orc, v3_layer):
+    cfg = wl.V3_PREFILL
+    u, toks = with_outliers(cfg, wl.tokens(cfg, "cuda"), n_tok=48)
+    check_layer(orc, cfg, tokens=list(toks) + [0, 1, cfg.T - 1], layer=v3_layer, u=u)
 
 
 @pytest.mark.parametrize("T", [1, 16, 64, 255, 256])

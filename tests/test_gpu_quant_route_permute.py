@@ -93,7 +93,8 @@ def route_case(L, orc, cfg, T=None):
     g = L.moe_route(inp["u"].cuda(), inp["centroids"].cuda(), inp["bias"].cuda(), cfg.K)
     torch.cuda.synchronize()
     r = orc.route(bits(inp["u"]), inp["centroids"].numpy(), inp["bias"].numpy(), cfg.K)
-    bad = routing_agreement(g["idx"].cpu().numpy(), g["gate"].cpu().numpy(), r)
+    bad = routing_agreement(g["idx"].cpu().numpy(), g["gate"].cpu().numpy(), r,
+                            bias=inp["bias"].numpy())
     counts = g["counts"].cpu().numpy()
     assert np.array_equal(counts, np.bincount(g["idx"].cpu().numpy().ravel(), minlength=cfg.E))
     if len(bad) == 0:

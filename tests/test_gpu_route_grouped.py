@@ -36,7 +36,7 @@ def _check(L, orc, cfg, u=None, b=None):
     r = orc.route_grouped(bits(u), inp["centroids"].numpy(), b.numpy(), cfg.K, cfg.n_groups,
                           cfg.topk_groups, cfg.group_topk)
     gidx = g["idx"].cpu().numpy()
-    bad = routing_agreement(gidx, g["gate"].cpu().numpy(), r)
+    bad = routing_agreement(gidx, g["gate"].cpu().numpy(), r, bias=b.numpy())
     gsz = cfg.E // cfg.n_groups
     assert all(len(set((row // gsz).tolist())) <= cfg.topk_groups for row in gidx)
     counts = g["counts"].cpu().numpy()
@@ -79,7 +79,8 @@ def test_forward_with_group_routing(orc):
     u_cpu = u.cpu()
     r = orc.route_grouped(bits(u_cpu), wl.centroids(cfg).numpy(), wl.bias(cfg).numpy(), cfg.K,
                           cfg.n_groups, cfg.topk_groups, cfg.group_topk)
-    bad = routing_agreement(out["idx"].cpu().numpy(), out["gate"].cpu().numpy(), r)
+    bad = routing_agreement(out["idx"].cpu().numpy(), out["gate"].cpu().numpy(), r,
+                            bias=wl.bias(cfg).numpy())
     toks = np.array([t for t in range(cfg.T) if t not in set(bad.tolist())], np.int64)
     need = set(range(cfg.E, cfg.E + cfg.S)) | {int(e) for t in toks for e in r["idx"][t]}
     W = oracle_weights(orc, cfg, need)

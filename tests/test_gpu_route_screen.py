@@ -47,7 +47,7 @@ def _route_against_oracle(L, orc, u, c, b, K):
     g = L.moe_route(u.cuda(), c.cuda(), b.cuda(), K)
     torch.cuda.synchronize()
     r = orc.route(bits(u), c.numpy(), b.numpy(), K)
-    bad = routing_agreement(g["idx"].cpu().numpy(), g["gate"].cpu().numpy(), r)
+    bad = routing_agreement(g["idx"].cpu().numpy(), g["gate"].cpu().numpy(), r, bias=b.numpy())
     return g, r, bad
 
 
