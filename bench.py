@@ -354,6 +354,7 @@ def run_ours(args, world, rank, local):
     backward = run_backward(layer, cfg, dev, pk) if legs else None
     wgrad = run_wgrad(layer, cfg, dev, pk) if legs else None
     skew = run_skew(layer, dev, pk, fp8_sus) if legs else None
+    pipelined = run_pipelined(layer, cfg, dev) if legs else None
     balance = run_balance(layer, cfg, dev) if args.workload == "v3_long" else None
 
     line = {
@@ -378,6 +379,8 @@ def run_ours(args, world, rank, local):
         line["backward_wgrad"] = wgrad
     if skew:
         line["skew"] = skew
+    if pipelined:
+        line["pipelined"] = pipelined
     if legs:
         # the tensor-bound configuration: its own layer (weights of its seed), after
         # the prefill layer's memory is released
@@ -462,6 +465,44 @@ def run_skew(layer, dev, pk, fp8_sus, steps=50, warmup=5):
             "hot_fraction": round(hot, 3), "max_expert_rows": int(counts.max()),
             "gemm_gate_up_frac_of_hbm": round(gu["GBps"] / pk["hbm_gbs"], 4),
             "kernels": kernels}
+
+
+def run_pipelined(layer, cfg, dev, n_batches=12, reserves=(0, 8, 16, 24, 32)):
+    """Two micro-batches in flight (moe_forward_pipelined) against the same
+    batches run one after another (moe_forward + moe_update_bias each): ms per
+    batch for each number of SMs the GEMMs leave to the routing / dispatch /
+    combine of the other batch.  CUDA events on the current stream, which waits
+    for both of the pipeline's streams."""
+    us = [wl.tokens(cfg, dev, step=k % 4) for k in range(n_batches)]
+    outs = [dict(layer.outputs(cfg.T), u=u) for u in us]
+    saved = layer.bias.clone()
+
+    def timed(fn):
+        fn()                                    # warm-up (workspaces, streams)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / n_batches
+
+    def seq():
+        for o in outs:
+            layer.forward(o["u"], o)
+            layer.update_bias(o["counts"], cfg.T, cfg.gamma)
+
+    res = {"batches": n_batches, "sequential_ms_per_batch": round(timed(seq), 4)}
+    for r in reserves:
+        res[f"pipelined_reserve_{r}_ms_per_batch"] = round(
+            timed(lambda: layer.forward_pipelined(us, cfg.gamma, r, outs)), 4)
+    if layer.pipelined_status() != 0:
+        raise RuntimeError("device status flagged in the pipelined leg")
+    layer.bias.copy_(saved)
+    best = min((v, k) for k, v in res.items() if k.startswith("pipelined"))
+    res["best"] = best[1]
+    res["speedup_vs_sequential"] = round(res["sequential_ms_per_batch"] / best[0], 4)
+    return res
 
 
 def run_long(dev, pk, fp8_sus, fp8_src, steps=10, warmup=3):

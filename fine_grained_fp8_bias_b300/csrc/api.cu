@@ -10,6 +10,9 @@ namespace moe {
 namespace {
 thread_local int g_last_cuda_error = 0;
 std::atomic<uint64_t> g_launches{0};
+constexpr long long kDefaultWaitCycles = 4000000000LL;   // about 2 s of SM clock
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+std::atomic<int> g_stall{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -87,14 +90,19 @@ constexpr int kSmallDownT = 4;
 int launch_gemm_large(int mode, const uint8_t* A, const float* sa, int M_total, const int32_t* go,
                       int G, const uint8_t* W0, const uint8_t* W1, const float* sw0,
                       const float* sw1, int N, int Kdim, void* out, float* out_scales,
-                      int32_t* status, cudaStream_t st, int f32_group0, int f32_row0, float* out2) {
+                      int32_t* status, cudaStream_t st, int f32_group0, int f32_row0, float* out2,
+                      int counter_slot, bool counter_zeroed, int max_ctas) {
     return launch_grouped_gemm(mode, A, sa, M_total, go, G, W0, W1, sw0, sw1, N, Kdim, out,
-                               out_scales, status, st, nullptr, f32_group0, f32_row0, out2);
+                               out_scales, status, st, nullptr, f32_group0, f32_row0, out2,
+                               counter_slot, counter_zeroed, max_ctas);
 }
 
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+long long pipeline_wait_cycles() { return g_wait_cycles.load(std::memory_order_relaxed); }
+int pipeline_stall() { return g_stall.load(std::memory_order_relaxed); }
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -130,6 +138,12 @@ const char* moe_status_string(int status) {
 int moe_last_cuda_error(void) { return g_last_cuda_error; }
 
 uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+long long moe_set_pipeline_wait_limit(long long cycles) {
+    return g_wait_cycles.exchange(cycles > 0 ? cycles : kDefaultWaitCycles);
+}
+
+int moe_set_pipeline_stall(int on) { return g_stall.exchange(on ? 1 : 0); }
 
 size_t moe_workspace_size(const moe_layer_t* L, int T_max) {
     if (!L || T_max < 0 || L->d <= 0 || L->E <= 0 || L->K <= 0 || L->S < 0 || L->I <= 0) return 0;
@@ -309,7 +323,7 @@ int moe_grouped_gemm_fp8_down(const uint8_t* H, const float* sh, int M_total,
     if (!aligned16(H) || !aligned16(W) || !aligned16(y) || !aligned16(y_f32)) return MOE_ERR_MISALIGNED;
     const auto gemm = small_tiles ? launch_grouped_gemm_small : launch_gemm_large;
     return gemm(MOE_GEMM_DOWN, H, sh, M_total, group_offsets, G, W, nullptr, sw, nullptr, N, Kdim,
-                y, nullptr, status, S_(stream), f32_group0, f32_row0, y_f32);
+                y, nullptr, status, S_(stream), f32_group0, f32_row0, y_f32, 1, false, 0);
 }
 
 int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
@@ -330,11 +344,39 @@ int moe_combine(const uint16_t* u, const uint16_t* Y, const float* topk_gate,
 namespace moe {
 namespace {
 
-// moe_forward's body; reset_status = false keeps the status word of earlier
-// calls (moe_forward_host clears it once for its whole batch sequence).
-int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
-                 float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
-                 cudaStream_t st, bool reset_status) {
+// Pointers of one forward's workspace (the layout above).
+struct Fwd {
+    int32_t *status, *hist, *bbase, *go, *offsets, *perm, *inv_row;
+    void* route_ws;
+    uint8_t *A, *H;
+    float *sa, *sh, *Ysh;
+    uint16_t* Y;
+};
+
+Fwd fwd_ptrs(const moe_layer_t* L, int T, void* ws) {
+    const Layout W = layout(T, L->d, L->E, L->K, L->S, L->I);
+    char* base = static_cast<char*>(ws);
+    Fwd f;
+    f.status = reinterpret_cast<int32_t*>(base + W.status);
+    f.route_ws = base + W.route;
+    f.hist = reinterpret_cast<int32_t*>(base + W.hist);
+    f.bbase = reinterpret_cast<int32_t*>(base + W.base);
+    f.go = reinterpret_cast<int32_t*>(base + W.go);
+    f.offsets = reinterpret_cast<int32_t*>(base + W.offsets);
+    f.perm = reinterpret_cast<int32_t*>(base + W.perm);   // T*(K+S) rows
+    f.inv_row = reinterpret_cast<int32_t*>(base + W.inv_row);
+    f.A = reinterpret_cast<uint8_t*>(base + W.A);
+    f.sa = reinterpret_cast<float*>(base + W.sa);
+    f.H = reinterpret_cast<uint8_t*>(base + W.H);
+    f.sh = reinterpret_cast<float*>(base + W.sh);
+    f.Y = reinterpret_cast<uint16_t*>(base + W.Y);
+    f.Ysh = reinterpret_cast<float*>(base + W.Ysh);
+    return f;
+}
+
+// Host-side checks shared by the forward entry points.
+int check_forward(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
+                  float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes) {
     int rc = check_layer(L);
     if (rc) return rc;
     if (T < 0) return MOE_ERR_INVALID_ARG;
@@ -343,53 +385,73 @@ int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, i
     if (T > 0 && (!u || !h_out || !topk_idx || !topk_gate || !tie_flag)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(u) || !aligned16(h_out)) return MOE_ERR_MISALIGNED;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
-    const int d = L->d, E = L->E, K = L->K, S = L->S, I = L->I, G = E + S;
-    const Layout W = layout(T, d, E, K, S, I);
-    if (ws_bytes < W.total) return MOE_ERR_WORKSPACE;
-    char* base = static_cast<char*>(ws);
-    int32_t* status = reinterpret_cast<int32_t*>(base + W.status);
-    void* route_ws = base + W.route;
-    int32_t* hist = reinterpret_cast<int32_t*>(base + W.hist);
-    int32_t* bbase = reinterpret_cast<int32_t*>(base + W.base);
-    int32_t* go = reinterpret_cast<int32_t*>(base + W.go);
-    int32_t* offsets = reinterpret_cast<int32_t*>(base + W.offsets);
-    int32_t* perm = reinterpret_cast<int32_t*>(base + W.perm);   // T*(K+S) rows
-    int32_t* inv_row = reinterpret_cast<int32_t*>(base + W.inv_row);
-    uint8_t* A = reinterpret_cast<uint8_t*>(base + W.A);
-    float* sa = reinterpret_cast<float*>(base + W.sa);
-    uint8_t* H = reinterpret_cast<uint8_t*>(base + W.H);
-    float* sh = reinterpret_cast<float*>(base + W.sh);
-    uint16_t* Y = reinterpret_cast<uint16_t*>(base + W.Y);
-    float* Ysh = reinterpret_cast<float*>(base + W.Ysh);
-    const int M = T * (K + S);
+    if (ws_bytes < layout(T, L->d, L->E, L->K, L->S, L->I).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
 
-    if (reset_status) {
-        const cudaError_t e = cudaMemsetAsync(status, 0, 16, st);
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
+// Phase 1 of a forward: status word, routing, dispatch, quantisation.
+// reset_status = false keeps status[0] (the device errors of earlier calls);
+// status[1] and status[2], the two GEMMs' tile counters, are always zeroed
+// here, so that no memset sits between the layer's kernels.
+int forward_prep(const moe_layer_t* L, const uint16_t* u, int T, int32_t* topk_idx,
+                 float* topk_gate, int32_t* counts, uint8_t* tie_flag, const Fwd& f,
+                 cudaStream_t st, bool reset_status) {
+    const int d = L->d, E = L->E, K = L->K, S = L->S;
+    int rc;
+    const cudaError_t e = reset_status ? cudaMemsetAsync(f.status, 0, 16, st)
+                                       : cudaMemsetAsync(f.status + 1, 0, 12, st);
+    if (e != cudaSuccess) return cuda_fail(e);
     if ((rc = launch_route_layer(u, L->centroids, L->bias, T, d, E, K, topk_idx, topk_gate, tie_flag,
-                                 counts, route_ws, status, st, L->n_groups, L->topk_groups,
+                                 counts, f.route_ws, f.status, st, L->n_groups, L->topk_groups,
                                  L->group_topk)))
         return rc;
     if (T == 0) return MOE_OK;
-    if ((rc = launch_permute(topk_idx, T, K, E, offsets, perm, inv_row, go, S, status, hist, bbase,
-                             st)))
+    if ((rc = launch_permute(topk_idx, T, K, E, f.offsets, f.perm, f.inv_row, f.go, S, f.status,
+                             f.hist, f.bbase, st)))
         return rc;
-    if ((rc = launch_quant_dispatch(u, T, d, inv_row, K, S, A, sa, M, status, st))) return rc;
+    return launch_quant_dispatch(u, T, d, f.inv_row, K, S, f.A, f.sa, T * (K + S), f.status, st);
+}
+
+// Phase 2: the two expert GEMMs (max_ctas > 0 caps their persistent grids).
+int forward_gemms(const moe_layer_t* L, int T, const Fwd& f, cudaStream_t st, int max_ctas) {
+    if (T == 0) return MOE_OK;
+    const int d = L->d, E = L->E, K = L->K, S = L->S, I = L->I, G = E + S;
+    const int M = T * (K + S);
     // Few tokens: no group has more than T rows, so the weight panels dominate
     // the bytes and the tiles of 128 weight rows x 32 rows keep more of them in
     // flight per SM (gemm_small.cu).  Routed rows of y in bf16, shared rows
     // (weight 1 in h') in float32.
     const auto gemm = T <= kSmallGemmT ? launch_grouped_gemm_small : launch_gemm_large;
     const auto gemm_down = T <= kSmallDownT ? launch_grouped_gemm_small : launch_gemm_large;
-    if ((rc = gemm(MOE_GEMM_GATE_UP_SILU_QUANT, A, sa, M, go, G, L->w_gate, L->w_up, L->s_gate,
-                   L->s_up, I, d, H, sh, status, st, 1 << 30, 0, nullptr)))
+    int rc;
+    if ((rc = gemm(MOE_GEMM_GATE_UP_SILU_QUANT, f.A, f.sa, M, f.go, G, L->w_gate, L->w_up,
+                   L->s_gate, L->s_up, I, d, f.H, f.sh, f.status, st, 1 << 30, 0, nullptr, 1, true,
+                   max_ctas)))
         return rc;
     // routed groups' rows (the first T*K) to Y in bf16, shared groups' rows to Ysh in float32
-    if ((rc = gemm_down(MOE_GEMM_DOWN, H, sh, M, go, G, L->w_down, nullptr, L->s_down, nullptr, d,
-                        I, Y, nullptr, status, st, E, T * K, Ysh)))
+    return gemm_down(MOE_GEMM_DOWN, f.H, f.sh, M, f.go, G, L->w_down, nullptr, L->s_down, nullptr, d,
+                     I, f.Y, nullptr, f.status, st, E, T * K, f.Ysh, 2, true, max_ctas);
+}
+
+// Phase 3: h' = u + shared + gated routed outputs.
+int forward_combine(const moe_layer_t* L, const uint16_t* u, int T, const float* topk_gate,
+                    float* h_out, const Fwd& f, cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    return launch_combine(u, f.Y, topk_gate, f.inv_row, f.Ysh, T, L->d, L->K, L->S, h_out, st);
+}
+
+// moe_forward's body; reset_status = false keeps the status word of earlier
+// calls (moe_forward_host clears it once for its whole batch sequence).
+int forward_impl(const moe_layer_t* L, const uint16_t* u, int T, float* h_out, int32_t* topk_idx,
+                 float* topk_gate, int32_t* counts, uint8_t* tie_flag, void* ws, size_t ws_bytes,
+                 cudaStream_t st, bool reset_status) {
+    int rc = check_forward(L, u, T, h_out, topk_idx, topk_gate, counts, tie_flag, ws, ws_bytes);
+    if (rc) return rc;
+    const Fwd f = fwd_ptrs(L, T, ws);
+    if ((rc = forward_prep(L, u, T, topk_idx, topk_gate, counts, tie_flag, f, st, reset_status)))
         return rc;
-    return launch_combine(u, Y, topk_gate, inv_row, Ysh, T, d, K, S, h_out, st);
+    if ((rc = forward_gemms(L, T, f, st, 0))) return rc;
+    return forward_combine(L, u, T, topk_gate, h_out, f, st);
 }
 
 // Backward workspace: status, dy codes and scales, dH, [dG | dU] codes and
@@ -718,6 +780,62 @@ int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t*
         if ((e = cudaEventRecord(d2h_done[s], down)) != cudaSuccess) return cuda_fail(e);
     }
     return MOE_OK;
+}
+
+int moe_forward_pipelined(const moe_layer_t* L, int T, int n_batches,
+                          const moe_batch_buffers_t* batches, float gamma, void* ws0, void* ws1,
+                          size_t ws_bytes, int reserve_sms, void* gemm_stream, void* side_stream) {
+    int rc = check_layer(L);
+    if (rc) return rc;
+    if (T < 0 || n_batches < 0 || reserve_sms < 0) return MOE_ERR_INVALID_ARG;
+    if (n_batches == 0) return MOE_OK;
+    if (!batches) return MOE_ERR_INVALID_ARG;
+    void* wss[2] = {ws0, ws1};
+    for (int k = 0; k < n_batches; ++k) {
+        const moe_batch_buffers_t& b = batches[k];
+        if ((rc = check_forward(L, b.u, T, b.h, b.topk_idx, b.topk_gate, b.counts, b.tie_flag,
+                                wss[k & 1], ws_bytes)))
+            return rc;
+    }
+    int sms = 0, dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (reserve_sms >= sms) return MOE_ERR_INVALID_ARG;
+    const int gemm_ctas = sms - reserve_sms;
+    const cudaStream_t gs = S_(gemm_stream), ss = S_(side_stream);
+    EventSet ev;
+    cudaEvent_t* prep_done = ev.ev;        // [2] batch k's dispatch rows are ready
+    cudaEvent_t* gemm_done = ev.ev + 2;    // [2] batch k's expert outputs are ready
+    for (int i = 0; i < 4; ++i)
+        if ((e = cudaEventCreateWithFlags(&ev.ev[i], cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e);
+    Fwd f[2] = {fwd_ptrs(L, T, ws0), fwd_ptrs(L, T, ws1)};
+    // side stream: prep(0), prep(1), combine(0), prep(2), combine(1), ... ; the
+    // bias update of batch k sits between its routing and the next batch's, and
+    // a workspace is reused by batch k + 2 only after batch k's combine
+    auto combine = [&](int k) -> int {
+        const moe_batch_buffers_t& b = batches[k];
+        cudaError_t ce = cudaStreamWaitEvent(ss, gemm_done[k & 1], 0);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        return forward_combine(L, b.u, T, b.topk_gate, b.h, f[k & 1], ss);
+    };
+    for (int k = 0; k < n_batches; ++k) {
+        const moe_batch_buffers_t& b = batches[k];
+        const Fwd& fk = f[k & 1];
+        if ((rc = forward_prep(L, b.u, T, b.topk_idx, b.topk_gate, b.counts, b.tie_flag, fk, ss,
+                               k < 2)))
+            return rc;
+        if (gamma != 0.0f &&
+            (rc = launch_update_bias(b.counts, L->E, T, L->K, gamma, const_cast<float*>(L->bias), ss)))
+            return rc;
+        if ((e = cudaEventRecord(prep_done[k & 1], ss)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamWaitEvent(gs, prep_done[k & 1], 0)) != cudaSuccess) return cuda_fail(e);
+        if ((rc = forward_gemms(L, T, fk, gs, gemm_ctas))) return rc;
+        if ((e = cudaEventRecord(gemm_done[k & 1], gs)) != cudaSuccess) return cuda_fail(e);
+        if (k >= 1 && (rc = combine(k - 1))) return rc;
+    }
+    return combine(n_batches - 1);
 }
 
 int moe_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,

@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       float* __restrict__ h) {
     __shared__ int rows[kMaxTopK];
     __shared__ float gs[kMaxTopK];
+    griddep_wait();
+    griddep_launch();
     const int chunk = blockDim.x * 8;
     const int nch = (d + chunk - 1) / chunk;
     const long long items = (long long)T * nch;
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 __global__ void update_bias_kernel(const int32_t* __restrict__ counts, int E, long long n,
                                    float gamma, float* __restrict__ bias) {
+    griddep_wait();
+    griddep_launch();
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
         const long long load = (long long)counts[e] * E;
         if (load > n)
@@ -96,8 +100,8 @@ int launch_combine_t(const uint16_t* u, const uint16_t* Y, const float* gate, co
     const int threads = 128;
     const long long items = (long long)T * ((d + threads * 8 - 1) / (threads * 8));
     const int blocks = (int)(items < 148 * 16 ? items : 148 * 16);
-    combine_kernel<YST><<<blocks, threads, 0, st>>>(u, Y, gate, inv_row, Ysh, T, d, K, S, h);
-    return check_launch();
+    return launch_pdl(combine_kernel<YST>, dim3(blocks), dim3(threads), 0, st, u, Y, gate, inv_row,
+                      Ysh, T, d, K, S, h);
 }
 
 int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,
@@ -112,8 +116,8 @@ int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, cons
 
 int launch_update_bias(const int32_t* counts, int E, int T, int K, float gamma, float* bias,
                        cudaStream_t st) {
-    update_bias_kernel<<<(E + 255) / 256, 256, 0, st>>>(counts, E, (long long)T * K, gamma, bias);
-    return check_launch();
+    return launch_pdl(update_bias_kernel, dim3((E + 255) / 256), dim3(256), 0, st, counts, E,
+                      (long long)T * K, gamma, bias);
 }
 
 }  // namespace moe

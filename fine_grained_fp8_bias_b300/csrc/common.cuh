@@ -11,6 +11,11 @@ namespace moe {
 
 // Counts every kernel this library launches (reported by moe_kernel_launches).
 void note_launch();
+// Limit of the grouped GEMMs' pipeline waits in SM clock cycles
+// (moe_set_pipeline_wait_limit; about 2 s by default).
+long long pipeline_wait_cycles();
+// Test switch of moe_set_pipeline_stall: the GEMM producers issue no loads.
+int pipeline_stall();
 // Records a failed CUDA call for moe_last_cuda_error and returns MOE_ERR_CUDA.
 int cuda_fail(cudaError_t e);
 // Checks the launch that was just made.
@@ -42,6 +47,39 @@ __device__ __forceinline__ float tile_scale(float amax) {
 
 __device__ __forceinline__ void flag_status(int32_t* status, int code) {
     if (status) atomicCAS(status, 0, code);
+}
+
+// Programmatic dependent launch.  The kernels of the layer are launched with
+// launch_pdl, so a kernel's CTAs can be scheduled while the previous kernel
+// in the stream drains.  Every kernel therefore calls griddep_wait() before
+// its first access to global memory (it returns once the previous kernel has
+// completed and its writes are visible; without a programmatic predecessor
+// it returns at once), then griddep_launch() so that the next kernel can be
+// scheduled.  Correctness never depends on griddep_launch(): the next
+// kernel's own griddep_wait() waits for this whole grid.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel` on `st` with programmatic stream serialization allowed
+// (see griddep_wait); counts the launch and checks it.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+               Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    note_launch();
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -96,20 +134,25 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, in
                    int32_t* inv_row, int32_t* group_offsets_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st);
 // DOWN modes: with out2 set, the rows of groups >= f32_group0 are stored as
-// float32 in out2 (row - f32_row0) and the other rows as bf16 in out.
+// float32 in out2 (row - f32_row0) and the other rows as bf16 in out.  The
+// tile counter is status[counter_slot], zeroed by the launcher unless
+// counter_zeroed says the caller has.  max_ctas > 0 caps the persistent grid
+// (the SMs left free run other work concurrently).
 int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total,
                         const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                         const float* sw0, const float* sw1, int N, int Kdim, void* out,
                         float* out_scales, int32_t* status, cudaStream_t st,
                         const uint16_t* dH = nullptr, int f32_group0 = 1 << 30, int f32_row0 = 0,
-                        float* out2 = nullptr);
+                        float* out2 = nullptr, int counter_slot = 1, bool counter_zeroed = false,
+                        int max_ctas = 0);
 // The same GEMM with tiles of 128 weight rows x up to 32 rows of a group
 // (gemm_small.cu; GATE_UP_SILU_QUANT and DOWN modes): for groups with few rows.
 int launch_grouped_gemm_small(int mode, const uint8_t* A, const float* sa, int M_total,
                               const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                               const float* sw0, const float* sw1, int N, int Kdim, void* out,
                               float* out_scales, int32_t* status, cudaStream_t st,
-                              int f32_group0 = 1 << 30, int f32_row0 = 0, float* out2 = nullptr);
+                              int f32_group0 = 1 << 30, int f32_row0 = 0, float* out2 = nullptr,
+                              int counter_slot = 1, bool counter_zeroed = false, int max_ctas = 0);
 // The combine: routed rows Y bf16 with shared rows Ysh float32 (the forward),
 // or both bf16 (the input gradient's rows, gathered with gate = NULL).
 int launch_combine(const uint16_t* u, const uint16_t* Y, const float* gate, const int32_t* inv_row,

@@ -121,6 +121,8 @@ struct Params {
     int f32_group0;
     int f32_row0;
     float* out2;
+    long long wait_cycles;                      // limit of every pipeline wait (SM clock cycles)
+    int stall;                                  // test switch: the producer issues no loads
 };
 
 // ----------------------------------------------------------- tile lookup
@@ -162,17 +164,17 @@ __device__ __forceinline__ uint32_t quant4_rcp(float a, float b, float c, float 
 
 // The next tile index from the ring (-1: no more tiles); false when the wait
 // gave up.  Single-thread form (MMA issuer) and warp form.
-__device__ __forceinline__ bool take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status) {
+__device__ __forceinline__ bool take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status, long long limit) {
     const int slot = tpos % TILE_SLOTS;
-    if (!mbar_wait(&ctl->tile_full[slot], (tpos / TILE_SLOTS) & 1, &ctl->abort, status)) return false;
+    if (!mbar_wait(&ctl->tile_full[slot], (tpos / TILE_SLOTS) & 1, &ctl->abort, status, limit)) return false;
     tile = ctl->tile_ring[slot];
     mbar_arrive(&ctl->tile_empty[slot]);
     ++tpos;
     return true;
 }
-__device__ __forceinline__ bool warp_take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status) {
+__device__ __forceinline__ bool warp_take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status, long long limit) {
     const int slot = tpos % TILE_SLOTS;
-    if (!warp_wait(&ctl->tile_full[slot], (tpos / TILE_SLOTS) & 1, &ctl->abort, status)) return false;
+    if (!warp_wait(&ctl->tile_full[slot], (tpos / TILE_SLOTS) & 1, &ctl->abort, status, limit)) return false;
     tile = ctl->tile_ring[slot];
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->tile_empty[slot]);
@@ -190,6 +192,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmB0,
                             const __grid_constant__ CUtensorMap tmB1, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    griddep_wait();
+    griddep_launch();
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * SMEM_STAGE);
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (next >= total_tiles) next = -1;
                 const int slot = tpos % TILE_SLOTS;
                 if (!mbar_wait(&ctl->tile_empty[slot], ((tpos / TILE_SLOTS) & 1) ^ 1, &ctl->abort,
-                               p.status)) {
+                               p.status, p.wait_cycles)) {
                     ok = false;
                     break;
                 }
@@ -308,7 +312,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
-                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, &ctl->abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, &ctl->abort, p.status, p.wait_cycles)) { ok = false; break; }
+                    if (p.stall) {
+                        // test switch: nothing fills this stage, so this wait (and the
+                        // MMA issuer's) runs out after the wait limit
+                        mbar_wait(&ctl->full[s], ph, &ctl->abort, p.status, p.wait_cycles);
+                        ok = false;
+                        break;
+                    }
                     uint8_t* sA = smem + (size_t)s * SMEM_STAGE;
                     uint8_t* sB = sA + SMEM_A;
                     mbar_expect_tx(&ctl->full[s], bytes);
@@ -331,15 +342,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             int tile;
             while (ok) {
-                if (!take_tile(ctl, tpos, tile, p.status)) break;
+                if (!take_tile(ctl, tpos, tile, p.status, p.wait_cycles)) break;
                 if (tile < 0) break;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     const uint32_t buf = it & 1;
                     const uint32_t tph = (it >> 1) & 1;
-                    if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, &ctl->abort, p.status)) { ok = false; break; }
-                    if (!mbar_wait(&ctl->full[s], ph, &ctl->abort, p.status)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, &ctl->abort, p.status, p.wait_cycles)) { ok = false; break; }
+                    if (!mbar_wait(&ctl->full[s], ph, &ctl->abort, p.status, p.wait_cycles)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smem + (size_t)s * SMEM_STAGE);
                     const uint32_t b0 = a0 + SMEM_A;
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         int tile;
         while (ok) {
-            if (!warp_take_tile(ctl, tpos, tile, p.status)) { ok = false; break; }
+            if (!warp_take_tile(ctl, tpos, tile, p.status, p.wait_cycles)) { ok = false; break; }
             if (tile < 0) break;
             const Tile tl = find_tile(ctl, G, tile);
             const int g0 = ctl->go[tl.g];
@@ -389,7 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int slot = it % SCALE_SLOTS;
                 const uint32_t ph = (it / SCALE_SLOTS) & 1;
                 bool got = true;
-                if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, &ctl->abort, p.status);
+                if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, &ctl->abort, p.status, p.wait_cycles);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
                 // 4-byte asynchronous copies; rows outside the group are zero-filled
                 // (source size 0).  One commit group per slab; slab it - SCALE_LAG is
@@ -438,7 +449,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         int tile;
         for (; ok; ++tcount) {
-            if (!warp_take_tile(ctl, tpos, tile, p.status)) { ok = false; break; }
+            if (!warp_take_tile(ctl, tpos, tile, p.status, p.wait_cycles)) { ok = false; break; }
             if (tile < 0) break;
             const Tile tl = find_tile(ctl, G, tile);
             const int g0 = ctl->go[tl.g];
@@ -464,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // scales of slab `it` from the ring; false when the wait gave up
             auto take_scales = [&](uint32_t i, float& lo, float& hi) -> bool {
                 const int slot = i % SCALE_SLOTS;
-                if (!warp_wait(&ctl->sfull[slot], (i / SCALE_SLOTS) & 1, &ctl->abort, p.status)) return false;
+                if (!warp_wait(&ctl->sfull[slot], (i / SCALE_SLOTS) & 1, &ctl->abort, p.status, p.wait_cycles)) return false;
                 const ScaleSlot& sl = ctl->scales[slot];
                 const float sa = sl.sa[row];
                 lo = sa * (gate_up ? sl.sw[0] : sl.sw[wg]);
@@ -481,7 +492,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     float lo, hi;
                     if (!take_scales(it, lo, hi) ||
-                        !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status)) {
+                        !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -490,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             } else if (KB > 0) {
                 if (!take_scales(it, s_lo, s_hi) ||
-                    !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status)) {
+                    !warp_wait(&ctl->tfull[it & 1], (it >> 1) & 1, &ctl->abort, p.status, p.wait_cycles)) {
                     ok = false;
                 } else {
                     tc_fence_after();
@@ -516,7 +527,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float last_hi = s_hi;
                 if (kb + 1 < KB) {
                     if (!take_scales(it + 1, s_lo, s_hi) ||
-                        !warp_wait(&ctl->tfull[(it + 1) & 1], ((it + 1) >> 1) & 1, &ctl->abort, p.status)) {
+                        !warp_wait(&ctl->tfull[(it + 1) & 1], ((it + 1) >> 1) & 1, &ctl->abort, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -574,7 +585,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->xbar);
-                if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status)) { ok = false; break; }
+                if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status, p.wait_cycles)) { ok = false; break; }
                 amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
                 if constexpr (dgrad) amax2 = fmaxf(ctl->amax_y[par][0][row], ctl->amax_y[par][1][row]);
                 // GATE_UP: one 1x128 block of h (columns 128 nt ..); gradient mode: the
@@ -650,7 +661,8 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
                         const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                         const float* sw0, const float* sw1, int N, int Kdim, void* out,
                         float* out_scales, int32_t* status, cudaStream_t st, const uint16_t* dH,
-                        int f32_group0, int f32_row0, float* out2) {
+                        int f32_group0, int f32_row0, float* out2, int counter_slot,
+                        bool counter_zeroed, int max_ctas) {
     if (M_total == 0 || G == 0) return MOE_OK;
     static int sm_count = 0;
     static std::once_flag once;
@@ -692,10 +704,11 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
     } else {
         mB1 = mB0;
     }
-    // status[1] is this call's tile counter (dynamic schedule); without a
-    // status buffer the tiles are taken in a fixed order
-    int* counter = status ? status + 1 : nullptr;
-    if (counter) {
+    // status[counter_slot] is this call's tile counter (dynamic schedule; zeroed
+    // here unless the caller already did); without a status buffer the tiles
+    // are taken in a fixed order
+    int* counter = status ? status + counter_slot : nullptr;
+    if (counter && !counter_zeroed) {
         const cudaError_t ce = cudaMemsetAsync(counter, 0, sizeof(int), st);
         if (ce != cudaSuccess) return cuda_fail(ce);
     }
@@ -705,17 +718,15 @@ int launch_grouped_gemm(int mode, const uint8_t* A, const float* sa, int M_total
         out2 = static_cast<float*>(out);
     }
     Params p{mode, M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter, dH,
-             down && out2 ? f32_group0 : (1 << 30), f32_row0, out2};
+             down && out2 ? f32_group0 : (1 << 30), f32_row0, out2, pipeline_wait_cycles(),
+             pipeline_stall()};
     const int NT = gu ? N / 128 : (N + BN - 1) / BN;
     const long long max_tiles = ((long long)(M_total + BM - 1) / BM + G) * NT;
-    const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);
-    if (kmode == 1)
-        grouped_gemm_fp8_kernel<1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
-    else if (kmode == 2)
-        grouped_gemm_fp8_kernel<2><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
-    else
-        grouped_gemm_fp8_kernel<0><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, p);
-    return check_launch();
+    const int ctas = max_ctas > 0 && max_ctas < sm_count ? max_ctas : sm_count;
+    const int grid = (int)(max_tiles < ctas ? max_tiles : ctas);
+    auto kernel = kmode == 1 ? grouped_gemm_fp8_kernel<1>
+                  : kmode == 2 ? grouped_gemm_fp8_kernel<2> : grouped_gemm_fp8_kernel<0>;
+    return launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, mA, mB0, mB1, p);
 }
 
 }  // namespace moe

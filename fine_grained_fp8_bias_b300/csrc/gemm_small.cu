@@ -113,6 +113,8 @@ struct SParams {
     int f32_group0;                              // DOWN: rows of groups >= f32_group0 go to
     int f32_row0;                                // out2 (float32, row - f32_row0), the others
     float* out2;                                 // to out (bf16)
+    long long wait_cycles;                       // limit of every pipeline wait (SM clock cycles)
+    int stall;                                   // test switch: the producer issues no loads
 };
 
 struct STile {
@@ -140,18 +142,18 @@ __device__ __forceinline__ float s_div_rcp(float x, float scale, float r) {
     return copysignf(fmaf(fmaf(-scale, q1, x), r, q1), x);
 }
 
-__device__ __forceinline__ bool s_take_tile(SCtl* ctl, uint32_t& tpos, int& tile, int32_t* status) {
+__device__ __forceinline__ bool s_take_tile(SCtl* ctl, uint32_t& tpos, int& tile, int32_t* status, long long limit) {
     const int slot = tpos % S_TILE_SLOTS;
-    if (!mbar_wait(&ctl->tile_full[slot], (tpos / S_TILE_SLOTS) & 1, &ctl->abort, status)) return false;
+    if (!mbar_wait(&ctl->tile_full[slot], (tpos / S_TILE_SLOTS) & 1, &ctl->abort, status, limit)) return false;
     tile = ctl->tile_ring[slot];
     mbar_arrive(&ctl->tile_empty[slot]);
     ++tpos;
     return true;
 }
 __device__ __forceinline__ bool s_warp_take_tile(SCtl* ctl, uint32_t& tpos, int& tile,
-                                                 int32_t* status) {
+                                                 int32_t* status, long long limit) {
     const int slot = tpos % S_TILE_SLOTS;
-    if (!warp_wait(&ctl->tile_full[slot], (tpos / S_TILE_SLOTS) & 1, &ctl->abort, status)) return false;
+    if (!warp_wait(&ctl->tile_full[slot], (tpos / S_TILE_SLOTS) & 1, &ctl->abort, status, limit)) return false;
     tile = ctl->tile_ring[slot];
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->tile_empty[slot]);
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     using C = SmallCfg<MODE>;
     constexpr bool gate_up = MODE != 0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    griddep_wait();
+    griddep_launch();
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     SCtl* ctl = reinterpret_cast<SCtl*>(smem + (size_t)C::STAGES * C::STAGE);
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 if (next >= total_tiles) next = -1;
                 const int slot = tpos % S_TILE_SLOTS;
                 if (!mbar_wait(&ctl->tile_empty[slot], ((tpos / S_TILE_SLOTS) & 1) ^ 1, &ctl->abort,
-                               p.status))
+                               p.status, p.wait_cycles))
                     break;
                 ctl->tile_ring[slot] = next;
                 mbar_arrive(&ctl->tile_full[slot]);
@@ -264,7 +268,15 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 const uint32_t bytes = C::NW * SMEM_W + boxes * SBOX * SK;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % C::STAGES;
-                    if (!mbar_wait(&ctl->empty[s], ((it / C::STAGES) & 1) ^ 1, &ctl->abort, p.status)) {
+                    if (!mbar_wait(&ctl->empty[s], ((it / C::STAGES) & 1) ^ 1, &ctl->abort, p.status, p.wait_cycles)) {
+                        ok = false;
+                        break;
+                    }
+                    if (p.stall) {
+                        // test switch: nothing fills this stage, so this wait (and the
+                        // MMA issuer's) runs out after the wait limit
+                        mbar_wait(&ctl->full[s], (it / C::STAGES) & 1, &ctl->abort, p.status,
+                                  p.wait_cycles);
                         ok = false;
                         break;
                     }
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             uint32_t it = 0, tpos = 0;
             int tile;
             for (bool ok = true; ok;) {
-                if (!s_take_tile(ctl, tpos, tile, p.status) || tile < 0) break;
+                if (!s_take_tile(ctl, tpos, tile, p.status, p.wait_cycles) || tile < 0) break;
                 const STile tl = s_find_tile(ctl, G, NB, tile);
                 const int nv = min(STOK, ctl->go[tl.g + 1] - ctl->go[tl.g] - tl.c * STOK);
                 const int boxes = (nv + SBOX - 1) / SBOX;
@@ -294,8 +306,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % C::STAGES;
                     const uint32_t buf = it % S_NBUF;
-                    if (!mbar_wait(&ctl->tempty[buf], ((it / S_NBUF) & 1) ^ 1, &ctl->abort, p.status) ||
-                        !mbar_wait(&ctl->full[s], (it / C::STAGES) & 1, &ctl->abort, p.status)) {
+                    if (!mbar_wait(&ctl->tempty[buf], ((it / S_NBUF) & 1) ^ 1, &ctl->abort, p.status, p.wait_cycles) ||
+                        !mbar_wait(&ctl->full[s], (it / C::STAGES) & 1, &ctl->abort, p.status, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         bool ok = true;
         int tile;
         while (ok) {
-            if (!s_warp_take_tile(ctl, tpos, tile, p.status)) { ok = false; break; }
+            if (!s_warp_take_tile(ctl, tpos, tile, p.status, p.wait_cycles)) { ok = false; break; }
             if (tile < 0) break;
             const STile tl = s_find_tile(ctl, G, NB, tile);
             const int g0 = ctl->go[tl.g];
@@ -344,7 +356,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 bool got = true;
                 if (lane == 0)
                     got = mbar_wait(&ctl->sempty[slot], ((it / S_SCALE_SLOTS) & 1) ^ 1, &ctl->abort,
-                                    p.status);
+                                    p.status, p.wait_cycles);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
                 SScaleSlot& sl = ctl->scales[slot];
                 cp_async4(&sl.sa[lane], v ? p.sa + (size_t)kb * p.M_total + row : p.sa, v ? 4u : 0u);
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         bool ok = true;
         int tile;
         for (; ok; ++tcount) {
-            if (!s_warp_take_tile(ctl, tpos, tile, p.status)) { ok = false; break; }
+            if (!s_warp_take_tile(ctl, tpos, tile, p.status, p.wait_cycles)) { ok = false; break; }
             if (tile < 0) break;
             const STile tl = s_find_tile(ctl, G, NB, tile);
             const int g0 = ctl->go[tl.g];
@@ -385,8 +397,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int slot = it % S_SCALE_SLOTS;
                 const uint32_t buf = it % S_NBUF;
-                if (!warp_wait(&ctl->sfull[slot], (it / S_SCALE_SLOTS) & 1, &ctl->abort, p.status) ||
-                    !warp_wait(&ctl->tfull[buf], (it / S_NBUF) & 1, &ctl->abort, p.status)) {
+                if (!warp_wait(&ctl->sfull[slot], (it / S_SCALE_SLOTS) & 1, &ctl->abort, p.status, p.wait_cycles) ||
+                    !warp_wait(&ctl->tfull[buf], (it / S_NBUF) & 1, &ctl->abort, p.status, p.wait_cycles)) {
                     ok = false;
                     break;
                 }
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->xbar);
-                if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status)) { ok = false; break; }
+                if (!warp_wait(&ctl->xbar, (uint32_t)par, &ctl->abort, p.status, p.wait_cycles)) { ok = false; break; }
                 uint8_t* dst = static_cast<uint8_t*>(p.out) + (size_t)row0 * p.N + tl.nt * SWR + r;
 #pragma unroll
                 for (int t = 0; t < STOK; ++t) {
@@ -468,7 +480,8 @@ int launch_grouped_gemm_small(int mode, const uint8_t* A, const float* sa, int M
                               const int32_t* go, int G, const uint8_t* W0, const uint8_t* W1,
                               const float* sw0, const float* sw1, int N, int Kdim, void* out,
                               float* out_scales, int32_t* status, cudaStream_t st, int f32_group0,
-                              int f32_row0, float* out2) {
+                              int f32_row0, float* out2, int counter_slot, bool counter_zeroed,
+                              int max_ctas) {
     if (M_total == 0 || G == 0) return MOE_OK;
     static int sm_count = 0;
     static std::once_flag once;
@@ -493,8 +506,8 @@ int launch_grouped_gemm_small(int mode, const uint8_t* A, const float* sa, int M
     } else {
         mW1 = mW0;
     }
-    int* counter = status ? status + 1 : nullptr;
-    if (counter) {
+    int* counter = status ? status + counter_slot : nullptr;
+    if (counter && !counter_zeroed) {
         const cudaError_t ce = cudaMemsetAsync(counter, 0, sizeof(int), st);
         if (ce != cudaSuccess) return cuda_fail(ce);
     }
@@ -504,14 +517,16 @@ int launch_grouped_gemm_small(int mode, const uint8_t* A, const float* sa, int M
         out2 = static_cast<float*>(out);
     }
     SParams p{M_total, G, N, Kdim, go, sa, sw0, sw1, out, out_scales, status, counter,
-              !gu && out2 ? f32_group0 : (1 << 30), f32_row0, out2};
+              !gu && out2 ? f32_group0 : (1 << 30), f32_row0, out2, pipeline_wait_cycles(),
+              pipeline_stall()};
     const long long max_tiles = ((long long)(M_total + STOK - 1) / STOK + G) * (N / SWR);
-    const int grid = (int)(max_tiles < sm_count ? max_tiles : sm_count);
+    const int ctas = max_ctas > 0 && max_ctas < sm_count ? max_ctas : sm_count;
+    const int grid = (int)(max_tiles < ctas ? max_tiles : ctas);
     if (gu)
-        grouped_gemm_small_kernel<1><<<grid, S_THREADS, small_smem_bytes<1>(), st>>>(mA, mW0, mW1, p);
-    else
-        grouped_gemm_small_kernel<0><<<grid, S_THREADS, small_smem_bytes<0>(), st>>>(mA, mW0, mW1, p);
-    return check_launch();
+        return launch_pdl(grouped_gemm_small_kernel<1>, dim3(grid), dim3(S_THREADS),
+                          small_smem_bytes<1>(), st, mA, mW0, mW1, p);
+    return launch_pdl(grouped_gemm_small_kernel<0>, dim3(grid), dim3(S_THREADS),
+                      small_smem_bytes<0>(), st, mA, mW0, mW1, p);
 }
 
 }  // namespace moe

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
                                                    int E, int32_t* __restrict__ hist,
                                                    int32_t* status) {
     extern __shared__ int32_t h[];
+    griddep_wait();
+    griddep_launch();
     for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
     __syncthreads();
     const int t0 = blockIdx.x * kPermuteChunk;
@@ -45,6 +47,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ go_ext) {
     __shared__ int32_t warp_sums[32];
+    griddep_wait();
+    griddep_launch();
     const int tid = threadIdx.x;
     int total = 0;
     if (tid < E)
@@ -94,6 +98,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
                                                       int32_t* __restrict__ perm,
                                                       int32_t* __restrict__ inv_row) {
     extern __shared__ int32_t sel[];            // this chunk's selections, (token, slot) order
+    griddep_wait();
+    griddep_launch();
     const int t0 = blockIdx.x * kPermuteChunk;
     const int t1 = min(T, t0 + kPermuteChunk);
     const int n = (t1 - t0) * K;
@@ -122,19 +128,17 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, in
                    int32_t* inv_row, int32_t* go_ext, int S, int32_t* status,
                    int32_t* ws_hist, int32_t* ws_base, cudaStream_t st) {
     const int nchunks = (T + kPermuteChunk - 1) / kPermuteChunk;
-    if (nchunks > 0) {
-        hist_kernel<<<nchunks, 256, sizeof(int32_t) * E, st>>>(idx, T, K, E, ws_hist, status);
-        int rc = check_launch();
-        if (rc) return rc;
-    }
-    scan_kernel<<<1, 1024, 0, st>>>(ws_hist, nchunks, E, T, K, S, ws_base, offsets, go_ext);
-    int rc = check_launch();
-    if (rc) return rc;
-    if (nchunks > 0) {
-        scatter_kernel<<<nchunks, 256, sizeof(int32_t) * kPermuteChunk * K, st>>>(
-            idx, T, K, E, S, ws_base, perm, inv_row);
-        rc = check_launch();
-    }
+    int rc;
+    if (nchunks > 0 && (rc = launch_pdl(hist_kernel, dim3(nchunks), dim3(256), sizeof(int32_t) * E,
+                                        st, idx, T, K, E, ws_hist, status)))
+        return rc;
+    if ((rc = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, (const int32_t*)ws_hist, nchunks,
+                         E, T, K, S, ws_base, offsets, go_ext)))
+        return rc;
+    if (nchunks > 0)
+        rc = launch_pdl(scatter_kernel, dim3(nchunks), dim3(256),
+                        sizeof(int32_t) * kPermuteChunk * K, st, idx, T, K, E, S,
+                        (const int32_t*)ws_base, perm, inv_row);
     return rc;
 }
 

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(
     const uint16_t* __restrict__ x, int n_src, const int32_t* __restrict__ gather, int n_gather,
     int tail_T, int M, int d, uint8_t* __restrict__ q, float* __restrict__ scales, int scale_ld,
     int32_t* status) {
+    griddep_wait();
+    griddep_launch();
     const int lane = threadIdx.x & 31;
     const int warps_per_block = blockDim.x >> 5;
     const int half = lane >> 4;          // which tile of the 256-wide step
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int d, const int32_t* __restrict__ inv_row, int K,
     int S, int M, uint8_t* __restrict__ q, float* __restrict__ scales, int scale_ld,
     int32_t* status) {
+    griddep_wait();
+    griddep_launch();
     const int lane = threadIdx.x & 31;
     const int warps_per_block = blockDim.x >> 5;
     const int half = lane >> 4;
@@ -189,10 +193,8 @@ int launch_quant_1x128(const uint16_t* x, int n_src, const int32_t* gather, int 
     const int warps = 8;
     int blocks = (M + warps - 1) / warps;
     if (blocks > 148 * 16) blocks = 148 * 16;
-    quant_1x128_kernel<<<blocks, warps * 32, 0, st>>>(x, n_src, gather, n_gather,
-                                                       tail_T > 0 ? tail_T : 1, M, d, q, scales,
-                                                       scale_ld, status);
-    return check_launch();
+    return launch_pdl(quant_1x128_kernel, dim3(blocks), dim3(warps * 32), 0, st, x, n_src, gather,
+                      n_gather, tail_T > 0 ? tail_T : 1, M, d, q, scales, scale_ld, status);
 }
 
 int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_row, int K, int S,
@@ -202,9 +204,8 @@ int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_ro
     const int warps = 8;
     const long long items = (long long)T * ((d + 255) / 256);
     const int blocks = (int)((items + warps - 1) / warps < 148 * 16 ? (items + warps - 1) / warps : 148 * 16);
-    quant_dispatch_kernel<<<blocks, warps * 32, 0, st>>>(x, T, d, inv_row, K, S, T * (K + S), q,
-                                                          scales, scale_ld, status);
-    return check_launch();
+    return launch_pdl(quant_dispatch_kernel, dim3(blocks), dim3(warps * 32), 0, st, x, T, d, inv_row,
+                      K, S, T * (K + S), q, scales, scale_ld, status);
 }
 
 int launch_quant_128x128(const float* w, int R, int C, uint8_t* q, float* scales,

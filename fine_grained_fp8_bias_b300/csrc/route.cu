@@ -50,10 +50,16 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
 __global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict__ u,
                                                      const float* __restrict__ c, int T, int d,
                                                      int E, int split, float* __restrict__ l,
-                                                     float* __restrict__ part) {
+                                                     float* __restrict__ part,
+                                                     int32_t* __restrict__ counts) {
     __shared__ __align__(16) float us[LK][LT];
     __shared__ __align__(16) float cs[LK][LE];
+    griddep_wait();
+    griddep_launch();
     const int tid = threadIdx.x;
+    // the selection kernel that follows adds into counts
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int e = tid; e < E; e += blockDim.x) counts[e] = 0;
     const int t0 = blockIdx.x * LT, e0 = blockIdx.y * LE;
     const int steps = d / LK;
     const int s_begin = (int)((long long)steps * blockIdx.z / split);
@@ -151,9 +157,13 @@ __global__ void __launch_bounds__(256) logits_kernel(const uint16_t* __restrict_
 constexpr int kSmallT = 8;
 __global__ void __launch_bounds__(128) logits_small_kernel(const uint16_t* __restrict__ u,
                                                            const float* __restrict__ c, int T,
-                                                           int d, int E, float* __restrict__ l) {
+                                                           int d, int E, float* __restrict__ l,
+                                                           int32_t* __restrict__ counts) {
     __shared__ float wacc[4][kSmallT], wcmp[4][kSmallT];
+    griddep_wait();
+    griddep_launch();
     const int e = blockIdx.x;
+    if (threadIdx.x == 0) counts[e] = 0;        // the selection kernel that follows adds into counts
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* crow = c + (size_t)e * d + lane * 4;
     float acc[kSmallT], cmp[kSmallT], chain[kSmallT];
@@ -230,6 +240,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ l,
                                                    float* __restrict__ gate,
                                                    uint8_t* __restrict__ tie,
                                                    int32_t* __restrict__ counts) {
+    griddep_wait();
+    griddep_launch();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -308,12 +320,12 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ l,
 }
 
 template <int NV>
-void launch_topk_nv(const float* l, const float* part, int split, const float* bias, int T, int E,
-                    int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts,
-                    cudaStream_t st) {
+int launch_topk_nv(const float* l, const float* part, int split, const float* bias, int T, int E,
+                   int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts,
+                   cudaStream_t st) {
     const int warps = 8;
-    topk_kernel<NV><<<(T + warps - 1) / warps, warps * 32, 0, st>>>(l, part, split, bias, T, E, K,
-                                                                     idx, gate, tie, counts);
+    return launch_pdl(topk_kernel<NV>, dim3((T + warps - 1) / warps), dim3(warps * 32), 0, st, l,
+                      part, split, bias, T, E, K, idx, gate, tie, counts);
 }
 
 }  // namespace
@@ -321,15 +333,18 @@ void launch_topk_nv(const float* l, const float* part, int split, const float* b
 int launch_route(const uint16_t* u, const float* cent, const float* bias, int T, int d, int E,
                  int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, float* logits,
                  cudaStream_t st, float* part, size_t part_floats) {
-    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (T == 0) return MOE_OK;
+    cudaError_t e;
+    if (T == 0) {
+        e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+    }
     int rc;
     const int gx = (T + LT - 1) / LT, gy = (E + LE - 1) / LE;
     int split = 1;
     if (T <= kSmallT) {
-        logits_small_kernel<<<E, 128, 0, st>>>(u, cent, T, d, E, logits);
-        if ((rc = check_launch())) return rc;
+        if ((rc = launch_pdl(logits_small_kernel, dim3(E), dim3(128), 0, st, u, cent, T, d, E, logits,
+                             counts)))
+            return rc;
         part = nullptr;
     } else {
         const int target = 2 * 148;
@@ -342,19 +357,18 @@ int launch_route(const uint16_t* u, const float* cent, const float* bias, int T,
             e = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
             if (e != cudaSuccess) return cuda_fail(e);
         }
-        logits_kernel<<<dim3(gx, gy, split), 256, 0, st>>>(u, cent, T, d, E, split, logits,
-                                                             use_part ? part : nullptr);
-        if ((rc = check_launch())) return rc;
+        if ((rc = launch_pdl(logits_kernel, dim3(gx, gy, split), dim3(256), 0, st, u, cent, T, d, E,
+                             split, logits, use_part ? part : nullptr, counts)))
+            return rc;
         if (!use_part) part = nullptr;
     }
     const int nv = (E + 31) / 32;
-    if (nv <= 1) launch_topk_nv<1>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 2) launch_topk_nv<2>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 4) launch_topk_nv<4>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 8) launch_topk_nv<8>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
-    else if (nv <= 16) launch_topk_nv<16>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
-    else launch_topk_nv<32>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
-    return check_launch();
+    if (nv <= 1) return launch_topk_nv<1>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    if (nv <= 2) return launch_topk_nv<2>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    if (nv <= 4) return launch_topk_nv<4>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    if (nv <= 8) return launch_topk_nv<8>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    if (nv <= 16) return launch_topk_nv<16>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
+    return launch_topk_nv<32>(logits, part, split, bias, T, E, K, idx, gate, tie, counts, st);
 }
 
 }  // namespace moe

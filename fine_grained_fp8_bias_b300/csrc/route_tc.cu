@@ -16,18 +16,20 @@
 //   2. logits_tc: l~ = u hi^T + u mid^T on the tensor cores
 //      (tcgen05.mma.kind::f16, bf16 operands, float32 accumulation in TMEM),
 //      split over d when there are few token tiles; partial sums to [split][T][E].
-//   3. select_refine, one block per token: |l~_e - l_e| is bounded by
+//   3. screen (one warp per token): |l~_e - l_e| is bounded by
 //      gamma |u_t| |c_e| (gamma = 2^-11 covers the split remainder and an error
 //      of one float32 ulp of the running sum per MMA instruction, with twofold
 //      headroom), and sigmoid has slope at most 1/4, so every biased score z_e
 //      lies in [lo_e, hi_e] around its estimate.  The K-th largest z is at
 //      least L_K, the K-th largest lo; an expert with hi_e < L_K - 2e-6 can
 //      neither be selected nor lie within 2e-6 of the K-th score, and every
-//      other expert is a candidate.  The candidates' logits are recomputed on
-//      CUDA cores with compensated summation (32-term FMA chains added with
-//      TwoSum), and the selection, gates and tie flag use those.  A token with
-//      more than 64 candidates (degenerate inputs: many equal scores)
-//      recomputes all E.
+//      other expert is a candidate.
+//   4. exact: the candidates' logits recomputed on CUDA cores with
+//      compensated summation (32-term FMA chains added with TwoSum), grouped
+//      by expert so that each centroid row is read once per block.
+//   5. select (one warp per token): selection, gates and tie flag from the
+//      exact logits.  A token with more than 64 candidates (degenerate inputs:
+//      many equal scores) recomputes all E there.
 // Selection order: descending s + b, equal scores broken by the lower expert
 // index.  Near-tie flag: the K-th and (K+1)-th biased scores differ by less
 // than 1e-6.
@@ -64,7 +66,7 @@ constexpr size_t RT_SMEM_BYTES = 1024 + (size_t)RT_STAGES * RT_STAGE + sizeof(Rt
 
 // Workspace: header (status word), centroid norms, hi, mid, partial logits.
 struct RouteWs {
-    size_t status, norms, hi, mid, part, total;
+    size_t status, norms, hi, mid, part, cand_n, cand_e, exact, bucket_cnt, bucket, total;
     int split;
 };
 
@@ -84,7 +86,12 @@ RouteWs route_ws(int T, int d, int E) {
     w.hi = align_up(w.norms + sizeof(float) * (size_t)E, 256);
     w.mid = align_up(w.hi + (size_t)E * d * 2, 256);
     w.part = align_up(w.mid + (size_t)E * d * 2, 256);
-    w.total = align_up(w.part + sizeof(float) * (size_t)w.split * T * E, 256);
+    w.cand_n = align_up(w.part + sizeof(float) * (size_t)w.split * T * E, 256);
+    w.cand_e = align_up(w.cand_n + sizeof(int32_t) * (size_t)T, 256);
+    w.exact = align_up(w.cand_e + sizeof(int32_t) * (size_t)T * CAND_CAP, 256);
+    w.bucket_cnt = align_up(w.exact + sizeof(float) * (size_t)T * CAND_CAP, 256);
+    w.bucket = align_up(w.bucket_cnt + sizeof(int32_t) * (size_t)E, 256);
+    w.total = align_up(w.bucket + sizeof(int32_t) * (size_t)E * T, 256);
     return w;
 }
 
@@ -107,11 +114,20 @@ __device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
 // One block per expert row: hi/mid pieces and |c_e| (times 1 + 2^-20 for its
 // own rounding) to norms[e].
 constexpr int SPLIT_THREADS = 256;
+// Block e also zeroes zero0[e] and zero1[e] (nullable): the counts and the
+// expert bucket sizes that later kernels of the same call add into.
 __global__ void __launch_bounds__(SPLIT_THREADS) split_centroids_kernel(
     const float* __restrict__ c, int E, int d, uint16_t* __restrict__ hi,
-    uint16_t* __restrict__ mid, float* __restrict__ norms) {
+    uint16_t* __restrict__ mid, float* __restrict__ norms, int32_t* __restrict__ zero0,
+    int32_t* __restrict__ zero1) {
     __shared__ float wsum[SPLIT_THREADS / 32];
+    griddep_wait();
+    griddep_launch();
     const int e = blockIdx.x;
+    if (threadIdx.x == 0) {
+        if (zero0) zero0[e] = 0;
+        if (zero1) zero1[e] = 0;
+    }
     float ss = 0.0f;
     for (int j = threadIdx.x * 4; j < d; j += SPLIT_THREADS * 4) {
         const size_t at = (size_t)e * d + j;
@@ -152,6 +168,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                      const __grid_constant__ CUtensorMap tmM, int T, int d, int E, int split,
                      float* __restrict__ part, int32_t* status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    griddep_wait();
+    griddep_launch();
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     RtCtl* ctl = reinterpret_cast<RtCtl*>(smem + (size_t)RT_STAGES * RT_STAGE);
@@ -330,32 +348,27 @@ __device__ __forceinline__ float kth_largest(const float (&z)[NV], int E, int K,
     return zk;
 }
 
-// One block of SEL_WARPS warps per token.  The token row goes to shared
-// memory once; warp 0 screens the estimates and lists the candidates (in
-// expert order); the warps share the candidates' exact dot products; warp 0
-// selects.  Dynamic shared memory: u_t [d] bf16, then the candidate list
-// (expert, s, z) of up to 32 * NV entries.
-template <int NV>
-__global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
-    const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
-    const float* __restrict__ part, int split, int T, int d, int E, int K,
-    const float* __restrict__ norms, int32_t* __restrict__ idx, float* __restrict__ gate,
-    uint8_t* __restrict__ tie, int32_t* __restrict__ counts) {
-    extern __shared__ __align__(16) uint8_t sel_sm[];
-    __shared__ float red[SEL_WARPS];
-    __shared__ int n_cand;
-    uint16_t* ut = reinterpret_cast<uint16_t*>(sel_sm);
-    int* ce = reinterpret_cast<int*>(sel_sm + (size_t)d * 2);
-    float* cs = reinterpret_cast<float*>(ce + NV * 32);
-    float* cz = cs + NV * 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t = blockIdx.x;
+// ------------------------------------------------------------ 3. screen / exact / select
+// The exact recomputation reorganised by expert, so that a centroid row read
+// once serves every token that has the expert as a candidate:
+//   screen  one warp per token: bounds of every biased score around its
+//           estimate, the candidates (in expert order) to cand_e[t][k], and
+//           each (token, slot) appended to its expert's bucket;
+//   exact   the buckets cut into equal runs of pairs; a block loads each
+//           expert's centroid row into shared memory once and its warps
+//           compute the candidates' logits (same compensated summation as
+//           exact_dot) into exact[t][k];
+//   select  one warp per token: sigmoid, selection, gates, tie flag, counts.
+// The order of the entries inside a bucket depends on timing, but every
+// (token, expert) logit is computed the same way wherever it lands, so the
+// results do not.  A token with more than CAND_CAP candidates (degenerate
+// inputs) computes all E logits in the select kernel.
 
-    // token row to shared memory, and |u_t|^2
+// |u_t|^2 by one warp (lane L takes 8 consecutive elements of every 256).
+__device__ __forceinline__ float warp_sumsq_bf16(const uint16_t* ut, int d, int lane) {
     float ss = 0.0f;
-    for (int j = threadIdx.x * 8; j < d; j += SEL_WARPS * 32 * 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(u + (size_t)t * d + j);
-        *reinterpret_cast<uint4*>(ut + j) = v;
+    for (int j = lane * 8; j < d; j += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(ut + j);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -366,90 +379,211 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_kernel(
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
+    return ss;
+}
 
+constexpr int SCR_WARPS = 8;
+template <int NV>
+__global__ void __launch_bounds__(SCR_WARPS * 32) screen_kernel(
+    const uint16_t* __restrict__ u, const float* __restrict__ bias, const float* __restrict__ part,
+    int split, int T, int d, int E, int K, const float* __restrict__ norms,
+    int32_t* __restrict__ cand_n, int32_t* __restrict__ cand_e, int32_t* __restrict__ bucket_cnt,
+    int32_t* __restrict__ bucket) {
+    griddep_wait();
+    griddep_launch();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * SCR_WARPS + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float ss = warp_sumsq_bf16(u + (size_t)t * d, d, lane);
+    const float gu = GAMMA * sqrtf(ss);
+    float lo[NV], hi[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int e = j * 32 + lane;
+        if (e < E) {
+            float l = 0.0f;
+            for (int q = 0; q < split; ++q) l += part[((size_t)q * T + t) * E + e];
+            const float za = sigmoid(l) + bias[e];
+            const float eps = 0.25f * gu * norms[e] + 1e-6f + 0x1p-22f * (fabsf(za) + 1.0f);
+            lo[j] = za - eps;
+            hi[j] = za + eps;
+        } else {
+            lo[j] = hi[j] = -FLT_MAX;
+        }
+    }
+    const float LK = kth_largest(lo, E, K, lane);
+    unsigned cand = 0;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+        if (j * 32 + lane < E && hi[j] >= LK - 2e-6f) cand |= 1u << j;
+    int n = __popc(cand);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    if (n > CAND_CAP) {                         // degenerate: the select kernel takes all E
+        if (lane == 0) cand_n[t] = -1;
+        return;
+    }
+    int base = 0;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const unsigned m = __ballot_sync(0xffffffffu, (cand >> j) & 1u);
+        if ((cand >> j) & 1u) {
+            const int e = j * 32 + lane;
+            const int k = base + __popc(m & ((1u << lane) - 1u));
+            cand_e[(size_t)t * CAND_CAP + k] = e;
+            const int pos = atomicAdd(&bucket_cnt[e], 1);
+            bucket[(size_t)e * T + pos] = t * CAND_CAP + k;
+        }
+        base += __popc(m);
+    }
+    if (lane == 0) cand_n[t] = n;
+}
+
+// l = u_t . c_e as exact_dot, with the token row read from global memory and
+// the centroid row from shared memory.
+__device__ __forceinline__ float exact_dot_gs(const uint16_t* __restrict__ ut, const float* cs,
+                                              int d, int lane) {
+    const int nblk = d / 128;
+    float acc = 0.0f, cmp = 0.0f;
+    for (int i = 0; i < nblk; i += 16) {
+        uint2 uv[16];                           // sixteen blocks' loads in flight
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (i + q < nblk) uv[q] = __ldg(reinterpret_cast<const uint2*>(ut + (i + q) * 128 + lane * 4));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {           // two chains of eight blocks, in order
+            if (i + 8 * h >= nblk) break;
+            float p = 0.0f;
+#pragma unroll
+            for (int q = 8 * h; q < 8 * h + 8; ++q) {
+                if (i + q < nblk) {
+                    const float4 cv = *reinterpret_cast<const float4*>(cs + (i + q) * 128 + lane * 4);
+                    p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].x & 0xFFFFu)), cv.x, p);
+                    p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].x >> 16)), cv.y, p);
+                    p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].y & 0xFFFFu)), cv.z, p);
+                    p = fmaf(bf16_bits_to_float(static_cast<uint16_t>(uv[q].y >> 16)), cv.w, p);
+                }
+            }
+            float err;
+            acc = two_sum(acc, p, err);
+            cmp += err;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float oa = __shfl_xor_sync(0xffffffffu, acc, off);
+        const float oc = __shfl_xor_sync(0xffffffffu, cmp, off);
+        float err;
+        acc = two_sum(acc, oa, err);
+        cmp = (cmp + oc) + err;
+    }
+    return acc + cmp;
+}
+
+constexpr int EX_WARPS = 8;
+// Dynamic shared memory: the centroid row [d] float, then the bucket offsets [E + 1].
+__global__ void __launch_bounds__(EX_WARPS * 32) exact_pairs_kernel(
+    const uint16_t* __restrict__ u, const float* __restrict__ c, int T, int d, int E,
+    const int32_t* __restrict__ bucket_cnt, const int32_t* __restrict__ bucket,
+    float* __restrict__ exact) {
+    extern __shared__ __align__(16) float ex_sm[];
+    griddep_wait();
+    griddep_launch();
+    float* cs = ex_sm;
+    int* offs = reinterpret_cast<int*>(ex_sm + d);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // exclusive scan of the bucket sizes (warp 0; E <= 1024)
     if (warp == 0) {
-        ss = 0.0f;
+        int carry = 0;
+        for (int b0 = 0; b0 < E; b0 += 32) {
+            const int e = b0 + lane;
+            const int v = e < E ? bucket_cnt[e] : 0;
+            int incl = v;
 #pragma unroll
-        for (int w = 0; w < SEL_WARPS; ++w) ss += red[w];
-        // approximate biased scores and the candidate band
-        float za[NV];
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int e = j * 32 + lane;
-            if (e < E) {
-                float l = 0.0f;
-                for (int s = 0; s < split; ++s) l += part[((size_t)s * T + t) * E + e];
-                za[j] = sigmoid(l) + bias[e];
-            } else {
-                za[j] = -FLT_MAX;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
             }
+            if (e < E) offs[e] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        // per-expert bounds [lo, hi] of the biased scores
-        const float gu = GAMMA * sqrtf(ss);
-        float lo[NV], hi[NV];
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int e = j * 32 + lane;
-            if (e < E) {
-                const float eps = 0.25f * gu * norms[e] + 1e-6f + 0x1p-22f * (fabsf(za[j]) + 1.0f);
-                lo[j] = za[j] - eps;
-                hi[j] = za[j] + eps;
-            } else {
-                lo[j] = hi[j] = -FLT_MAX;
-            }
-        }
-        const float LK = kth_largest(lo, E, K, lane);
-        unsigned cand = 0;
-#pragma unroll
-        for (int j = 0; j < NV; ++j)
-            if (j * 32 + lane < E && hi[j] >= LK - 2e-6f) cand |= 1u << j;
-        int n = __popc(cand);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-        if (n > CAND_CAP) {
-            cand = 0;
-#pragma unroll
-            for (int j = 0; j < NV; ++j)
-                if (j * 32 + lane < E) cand |= 1u << j;
-        }
-        // compact the candidates into ce[] in expert order
-        int base = 0;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const unsigned m = __ballot_sync(0xffffffffu, (cand >> j) & 1u);
-            if ((cand >> j) & 1u) ce[base + __popc(m & ((1u << lane) - 1u))] = j * 32 + lane;
-            base += __popc(m);
-        }
-        if (lane == 0) n_cand = base;
+        if (lane == 0) offs[E] = carry;
     }
     __syncthreads();
-
-    // exact scores of the candidates, shared among the warps
-    const int nc = n_cand;
-    for (int k = warp; k < nc; k += SEL_WARPS) {
-        const int e = ce[k];
-        const float l = exact_dot(ut, c + (size_t)e * d, d, lane);
-        if (lane == 0) {
-            const float sv = sigmoid(l);
-            cs[k] = sv;
-            cz[k] = sv + bias[e];
-        }
+    const int total = offs[E];
+    const int per = (total + gridDim.x - 1) / gridDim.x;
+    const int beg = min(total, (int)blockIdx.x * per);
+    const int end = min(total, beg + per);
+    if (beg >= end) return;
+    // first expert whose bucket holds pair index beg
+    int lo = 0, hi = E;                         // offs[lo] <= beg < offs[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offs[mid] <= beg) lo = mid; else hi = mid;
     }
-    __syncthreads();
-    if (warp != 0) return;
+    for (int e = lo, i0 = beg; i0 < end; ++e) {
+        const int s0 = max(i0, offs[e]), s1 = min(end, offs[e + 1]);
+        if (s0 >= s1) continue;
+        __syncthreads();                        // the previous row is no longer read
+        for (int j = threadIdx.x * 4; j < d; j += EX_WARPS * 32 * 4)
+            *reinterpret_cast<float4*>(cs + j) = __ldg(reinterpret_cast<const float4*>(c + (size_t)e * d + j));
+        __syncthreads();
+        for (int i = s0 + warp; i < s1; i += EX_WARPS) {
+            const int code = bucket[(size_t)e * T + (i - offs[e])];
+            const int t = code / CAND_CAP;
+            const float l = exact_dot_gs(u + (size_t)t * d, cs, d, lane);
+            if (lane == 0) exact[code] = l;
+        }
+        i0 = s1;
+    }
+}
 
-    // selection over the candidates
+constexpr int SEL2_WARPS = 8;
+template <int NV>
+__global__ void __launch_bounds__(SEL2_WARPS * 32) select_exact_kernel(
+    const uint16_t* __restrict__ u, const float* __restrict__ c, const float* __restrict__ bias,
+    int T, int d, int E, int K, const int32_t* __restrict__ cand_n,
+    const int32_t* __restrict__ cand_e, const float* __restrict__ exact,
+    int32_t* __restrict__ idx, float* __restrict__ gate, uint8_t* __restrict__ tie,
+    int32_t* __restrict__ counts) {
+    constexpr int NC = NV < 2 ? NV : 2;          // CAND_CAP = 64 candidates: two per lane
+    griddep_wait();
+    griddep_launch();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * SEL2_WARPS + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int n = cand_n[t];
     float s[NV], z[NV];
     int ex[NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-        const int k = j * 32 + lane;
-        if (k < nc) {
-            s[j] = cs[k]; z[j] = cz[k]; ex[j] = ce[k];
-        } else {
-            s[j] = 0.0f; z[j] = -FLT_MAX; ex[j] = 0x7fffffff;
+        s[j] = 0.0f;
+        z[j] = -FLT_MAX;
+        ex[j] = 0x7fffffff;
+    }
+    int nc;
+    if (n >= 0) {                               // the candidates' exact logits
+        nc = n;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            const int k = j * 32 + lane;
+            if (k < n) {
+                const int e = cand_e[(size_t)t * CAND_CAP + k];
+                const float sv = sigmoid(exact[(size_t)t * CAND_CAP + k]);
+                s[j] = sv;
+                z[j] = sv + bias[e];
+                ex[j] = e;
+            }
+        }
+    } else {                                    // every expert, exactly (degenerate inputs)
+        nc = E;
+        const uint16_t* ut = u + (size_t)t * d;
+        for (int e = 0; e < E; ++e) {
+            const float l = exact_dot(ut, c + (size_t)e * d, d, lane);
+            const float sv = sigmoid(l);
+#pragma unroll
+            for (int j = 0; j < NV; ++j)
+                if (e == j * 32 + lane) { s[j] = sv; z[j] = sv + bias[e]; ex[j] = e; }
         }
     }
     unsigned taken = 0;
@@ -514,6 +648,8 @@ __global__ void __launch_bounds__(SEL_WARPS * 32) select_refine_grouped_kernel(
     int topk_groups, int group_topk, const float* __restrict__ norms,
     int32_t* __restrict__ idx, float* __restrict__ gate, uint8_t* __restrict__ tie,
     int32_t* __restrict__ counts) {
+    griddep_wait();
+    griddep_launch();
     extern __shared__ __align__(16) uint8_t sel_sm[];
     __shared__ float red[SEL_WARPS];
     __shared__ int n_work;
@@ -769,25 +905,51 @@ int launch_select_grouped(const uint16_t* u, const float* c, const float* bias, 
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    select_refine_grouped_kernel<NV><<<T, SEL_WARPS * 32, smem, st>>>(
-        u, c, bias, part, split, T, d, E, K, n_groups, topk_groups, group_topk, norms, idx, gate,
-        tie, counts);
-    return check_launch();
+    return launch_pdl(select_refine_grouped_kernel<NV>, dim3(T), dim3(SEL_WARPS * 32), smem, st, u, c,
+                      bias, part, split, T, d, E, K, n_groups, topk_groups, group_topk, norms, idx,
+                      gate, tie, counts);
 }
 
+// Screen, exact recomputation by expert, selection (the workspace's candidate
+// lists, exact logits and expert buckets; see route_ws).
 template <int NV>
-int launch_select(const uint16_t* u, const float* c, const float* bias, const float* part,
-                  int split, int T, int d, int E, int K, const float* norms, int32_t* idx,
-                  float* gate, uint8_t* tie, int32_t* counts, cudaStream_t st) {
-    const size_t smem = (size_t)d * 2 + (size_t)NV * 32 * 12;
+int launch_select2(const uint16_t* u, const float* c, const float* bias, const float* part,
+                   int split, int T, int d, int E, int K, const float* norms, int32_t* idx,
+                   float* gate, uint8_t* tie, int32_t* counts, void* ws, cudaStream_t st) {
+    static int sm_count = 0;
+    if (sm_count == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (sm_count <= 0) sm_count = 148;
+    }
+    const RouteWs W = route_ws(T, d, E);
+    char* base = static_cast<char*>(ws);
+    int32_t* cand_n = reinterpret_cast<int32_t*>(base + W.cand_n);
+    int32_t* cand_e = reinterpret_cast<int32_t*>(base + W.cand_e);
+    float* exact = reinterpret_cast<float*>(base + W.exact);
+    int32_t* bucket_cnt = reinterpret_cast<int32_t*>(base + W.bucket_cnt);
+    int32_t* bucket = reinterpret_cast<int32_t*>(base + W.bucket);
+    // (bucket_cnt was zeroed by the split kernel of this call)
+    const int tb = (T + SCR_WARPS - 1) / SCR_WARPS;
+    int rc = launch_pdl(screen_kernel<NV>, dim3(tb), dim3(SCR_WARPS * 32), 0, st, u, bias, part,
+                        split, T, d, E, K, norms, cand_n, cand_e, bucket_cnt, bucket);
+    if (rc) return rc;
+    const size_t smem = sizeof(float) * (size_t)d + sizeof(int) * (size_t)(E + 1);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(select_refine_kernel<NV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const cudaError_t e = cudaFuncSetAttribute(
+            exact_pairs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    select_refine_kernel<NV><<<T, SEL_WARPS * 32, smem, st>>>(u, c, bias, part, split, T, d, E, K,
-                                                             norms, idx, gate, tie, counts);
-    return check_launch();
+    const long long pairs_max = (long long)T * (E < CAND_CAP ? E : CAND_CAP);
+    const long long want = 4LL * sm_count;
+    const int grid = (int)(pairs_max < want ? (pairs_max > 0 ? pairs_max : 1) : want);
+    if ((rc = launch_pdl(exact_pairs_kernel, dim3(grid), dim3(EX_WARPS * 32), smem, st, u, c, T, d, E,
+                         (const int32_t*)bucket_cnt, (const int32_t*)bucket, exact)))
+        return rc;
+    return launch_pdl(select_exact_kernel<NV>, dim3((T + SEL2_WARPS - 1) / SEL2_WARPS),
+                      dim3(SEL2_WARPS * 32), 0, st, u, c, bias, T, d, E, K, (const int32_t*)cand_n,
+                      (const int32_t*)cand_e, (const float*)exact, idx, gate, tie, counts);
 }
 
 // ------------------------------------------------------------ gate term
@@ -869,7 +1031,7 @@ __global__ void sum_partials_kernel(const float* __restrict__ part, int split, s
 // partial logit estimates.
 int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, void* ws,
                     int32_t* status, cudaStream_t st, const float** part_out, int* split_out,
-                    const float** norms_out) {
+                    const float** norms_out, int32_t* counts = nullptr) {
     const RouteWs W = route_ws(T, d, E);
     char* base = static_cast<char*>(ws);
     float* norms = reinterpret_cast<float*>(base + W.norms);
@@ -877,8 +1039,10 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
     uint16_t* mid = reinterpret_cast<uint16_t*>(base + W.mid);
     float* part = reinterpret_cast<float*>(base + W.part);
     int rc;
-    split_centroids_kernel<<<E, SPLIT_THREADS, 0, st>>>(cent, E, d, hi, mid, norms);
-    if ((rc = check_launch())) return rc;
+    int32_t* bucket_cnt = counts ? reinterpret_cast<int32_t*>(base + W.bucket_cnt) : nullptr;
+    if ((rc = launch_pdl(split_centroids_kernel, dim3(E), dim3(SPLIT_THREADS), 0, st, cent, E, d, hi,
+                         mid, norms, counts, bucket_cnt)))
+        return rc;
     static bool attr_set = false;
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(
@@ -891,9 +1055,9 @@ int estimate_logits(const uint16_t* u, const float* cent, int T, int d, int E, v
     if ((rc = make_map_2d(&mH, hi, (uint64_t)E, (uint64_t)d, 2, RT_N, RT_K))) return rc;
     if ((rc = make_map_2d(&mM, mid, (uint64_t)E, (uint64_t)d, 2, RT_N, RT_K))) return rc;
     const dim3 grid((T + RT_M - 1) / RT_M, (E + RT_N - 1) / RT_N, W.split);
-    logits_tc_kernel<<<grid, RT_THREADS, RT_SMEM_BYTES, st>>>(mU, mH, mM, T, d, E, W.split, part,
-                                                              status);
-    if ((rc = check_launch())) return rc;
+    if ((rc = launch_pdl(logits_tc_kernel, grid, dim3(RT_THREADS), RT_SMEM_BYTES, st, mU, mH, mM, T,
+                         d, E, W.split, part, status)))
+        return rc;
     *part_out = part;
     *split_out = W.split;
     *norms_out = norms;
@@ -966,13 +1130,14 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
                     int K, int32_t* idx, float* gate, uint8_t* tie, int32_t* counts, void* ws,
                     int32_t* status, cudaStream_t st, int n_groups, int topk_groups,
                     int group_topk) {
-    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (T == 0) return MOE_OK;
+    if (T == 0) {
+        const cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+    }
     const float* part;
     const float* norms;
     int split, rc;
-    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &norms))) return rc;
+    if ((rc = estimate_logits(u, cent, T, d, E, ws, status, st, &part, &split, &norms, counts))) return rc;
     const int nv = (E + 31) / 32;
     if (n_groups > 0) {
 #define MOE_GROUPED(N)                                                                          \
@@ -986,12 +1151,15 @@ int launch_route_tc(const uint16_t* u, const float* cent, const float* bias, int
         MOE_GROUPED(32);
 #undef MOE_GROUPED
     }
-    if (nv <= 1) return launch_select<1>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
-    if (nv <= 2) return launch_select<2>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
-    if (nv <= 4) return launch_select<4>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
-    if (nv <= 8) return launch_select<8>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
-    if (nv <= 16) return launch_select<16>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
-    return launch_select<32>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, st);
+#define MOE_SELECT(N) \
+    return launch_select2<N>(u, cent, bias, part, split, T, d, E, K, norms, idx, gate, tie, counts, ws, st)
+    if (nv <= 1) MOE_SELECT(1);
+    if (nv <= 2) MOE_SELECT(2);
+    if (nv <= 4) MOE_SELECT(4);
+    if (nv <= 8) MOE_SELECT(8);
+    if (nv <= 16) MOE_SELECT(16);
+    MOE_SELECT(32);
+#undef MOE_SELECT
 }
 
 }  // namespace moe

@@ -37,21 +37,24 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded waits: about 2 s of SM clock.  The clock is read only every 64
-// polls, so an unsatisfied wait costs little more than the poll itself.
-// On expiry the waiter records MOE_ERR_TIMEOUT, raises the CTA's abort flag
-// (which every other wait checks) and returns false.
+// Bounded waits: by default about 2 s of SM clock (the GEMMs take the limit
+// of their pipeline waits from the launch, see moe_set_pipeline_wait_limit).
+// The clock is read only every 64 polls, so an unsatisfied wait costs little
+// more than the poll itself.  On expiry the waiter records MOE_ERR_TIMEOUT,
+// raises the CTA's abort flag (which every other wait checks) and returns
+// false.
 constexpr long long WAIT_CYCLES = 4000000000LL;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* abort,
-                                          int32_t* status) {
+                                          int32_t* status, long long limit = WAIT_CYCLES) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
+    const uint32_t every = limit < 1000000 ? 0u : 63u;   // short limits: read the clock each poll
     for (uint32_t i = 1;; ++i) {
         if (mbar_test(bar, parity)) return true;
-        if ((i & 63) == 0) {
+        if ((i & every) == 0) {
             if (*reinterpret_cast<volatile int*>(abort)) return false;
-            if (clock64() - t0 > WAIT_CYCLES) {
+            if (clock64() - t0 > limit) {
                 atomicExch(abort, 1);
                 flag_status(status, MOE_ERR_TIMEOUT);
                 return false;
@@ -63,18 +66,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* a
 // any lane goes on (the epilogue's tcgen05.ld is .sync.aligned), and all
 // lanes agree on giving up.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* abort,
-                                          int32_t* status) {
+                                          int32_t* status, long long limit = WAIT_CYCLES) {
     const int lane = threadIdx.x & 31;
     const long long t0 = clock64();
+    const uint32_t every = limit < 1000000 ? 0u : 63u;
     for (uint32_t i = 0;; ++i) {
         const bool ready = mbar_test(bar, parity);
         if (__all_sync(0xffffffffu, ready)) return true;
-        if ((i & 63) == 63) {
+        if ((i & every) == every) {
             int stop = 0;
             if (lane == 0) {
                 if (*reinterpret_cast<volatile int*>(abort)) {
                     stop = 1;
-                } else if (clock64() - t0 > WAIT_CYCLES) {
+                } else if (clock64() - t0 > limit) {
                     atomicExch(abort, 1);
                     flag_status(status, MOE_ERR_TIMEOUT);
                     stop = 1;

@@ -116,6 +116,42 @@ class MoELayer:
                              *streams)
         return bufs
 
+    def forward_pipelined(self, us: list, gamma: float = 0.0, reserve_sms: int = 0,
+                          outs: list | None = None, streams=None) -> list:
+        """The layer over device-resident batches with two micro-batches in
+        flight (moe_forward_pipelined): batch k's routing and dispatch, and
+        batch k-1's combine, run on a side stream while the expert GEMMs of the
+        other batch run on the GEMM stream (their grids leave reserve_sms SMs
+        free).  With gamma != 0 the bias steps after every batch.  Returns the
+        per-batch output dicts; asynchronous on the two streams (the current
+        stream is made to wait for them)."""
+        if not us:
+            return []
+        T = us[0].shape[0]
+        outs = [dict(self.outputs(T), u=u) for u in us] if outs is None else outs
+        if getattr(self, "_ws2", None) is None or self._ws2.numel() < self.workspace(T).numel():
+            self._ws2 = torch.empty_like(self.workspace(T))
+        if streams is None:
+            streams = getattr(self, "_pipe_streams", None)
+            if streams is None:
+                streams = self._pipe_streams = (torch.cuda.Stream(self.device),
+                                                torch.cuda.Stream(self.device))
+        cur = torch.cuda.current_stream(self.device)
+        for s in streams:
+            s.wait_stream(cur)
+        lib.moe_forward_pipelined(self.struct(), outs, gamma, self.workspace(T), self._ws2,
+                                  reserve_sms, *streams)
+        for s in streams:
+            cur.wait_stream(s)
+        return outs
+
+    def pipelined_status(self, stream=None) -> int:
+        """Device status of the two workspaces of forward_pipelined (syncs)."""
+        a = self.status(stream)
+        ws = getattr(self, "_ws2", None)
+        b = lib.moe_check_device_status(ws[:16].view(torch.int32), stream) if ws is not None else 0
+        return a or b
+
     def capture_forward(self, u: torch.Tensor, out: dict | None = None):
         """A CUDA graph of moe_forward on the fixed buffers u and out (decode
         steps: the launches of one forward become one graph launch).  Refill u

@@ -60,6 +60,10 @@ def _load() -> ctypes.CDLL:
     lib.moe_last_cuda_error.restype = I32
     lib.moe_kernel_launches.restype = ctypes.c_uint64
     lib.moe_kernel_launches.argtypes = []
+    lib.moe_set_pipeline_wait_limit.restype = ctypes.c_longlong
+    lib.moe_set_pipeline_wait_limit.argtypes = [ctypes.c_longlong]
+    lib.moe_set_pipeline_stall.restype = I32
+    lib.moe_set_pipeline_stall.argtypes = [I32]
     lib.moe_last_cuda_error.argtypes = []
     lib.moe_workspace_size.restype = ctypes.c_size_t
     lib.moe_workspace_size.argtypes = [ctypes.POINTER(moe_layer_t), I32]
@@ -94,6 +98,9 @@ def _load() -> ctypes.CDLL:
         "moe_forward_host": [ctypes.POINTER(moe_layer_t), I32, I32, P, P, ctypes.c_float,
                              ctypes.POINTER(moe_batch_buffers_t), P, ctypes.c_size_t, P, P, P],
         "moe_check_device_status": [P, P],
+        "moe_forward_pipelined": [ctypes.POINTER(moe_layer_t), I32, I32,
+                                  ctypes.POINTER(moe_batch_buffers_t), ctypes.c_float, P, P,
+                                  ctypes.c_size_t, I32, P, P],
         "moe_wgrad_ld": [I32, I32],
         "moe_requant_128x1": [P, P, I32, I32, P, I32, P, P, I32, P, P],
         "moe_wgrad_gemm_fp8": [P, P, I32, P, P, I32, I32, P, I32, P, P, I32, P, P],
@@ -166,6 +173,18 @@ def _router_inputs(u: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor)
         raise ValueError(f"centroids {tuple(centroids.shape)} and bias {tuple(bias.shape)} "
                          f"do not match u {tuple(u.shape)}")
     return T, d, E
+
+
+def set_pipeline_wait_limit(cycles: int) -> int:
+    """Limit of the grouped GEMMs' pipeline waits in SM clock cycles for later
+    launches (<= 0: the default, about 2 s); returns the previous limit."""
+    return int(_lib.moe_set_pipeline_wait_limit(cycles))
+
+
+def set_pipeline_stall(on: bool) -> int:
+    """Test switch: grouped GEMMs launched afterwards issue no loads, so their
+    pipeline waits run out (MOE_ERR_TIMEOUT); returns the previous setting."""
+    return int(_lib.moe_set_pipeline_stall(1 if on else 0))
 
 
 def kernel_launches() -> int:
@@ -469,6 +488,31 @@ def moe_forward_host(L: moe_layer_t, T: int, u_host: list, h_host: list, gamma: 
                                  ctypes.cast(h_arr, P), gamma, b_arr, _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(compute_stream),
                                  _stream(h2d_stream), _stream(d2h_stream)), "moe_forward_host")
+
+
+def moe_forward_pipelined(L: moe_layer_t, batches: list, gamma: float, ws0: torch.Tensor,
+                          ws1: torch.Tensor, reserve_sms: int = 0, gemm_stream=None,
+                          side_stream=None) -> None:
+    """moe_forward_pipelined: batches is a list of dicts of device tensors
+    (u, h, idx, gate, tie, counts), all with the same T; two micro-batches are
+    in flight (one in its expert GEMMs, the other in routing/dispatch or
+    combine).  Asynchronous: synchronise side_stream before reading outputs."""
+    n = len(batches)
+    if n == 0:
+        return
+    T = batches[0]["u"].shape[0]
+    for b in batches:
+        _bits(b["u"], torch.bfloat16)
+        _dev(b["u"], "u")
+        if b["u"].shape[0] != T:
+            raise ValueError("every batch needs the same number of tokens")
+    arr = (moe_batch_buffers_t * n)(*[moe_batch_buffers_t(_ptr(b["u"]), _ptr(b["h"]), _ptr(b["idx"]),
+                                                          _ptr(b["gate"]), _ptr(b["tie"]),
+                                                          _ptr(b["counts"])) for b in batches])
+    nbytes = min(ws0.numel() * ws0.element_size(), ws1.numel() * ws1.element_size())
+    _check(_lib.moe_forward_pipelined(ctypes.byref(L), T, n, arr, gamma, _ptr(ws0), _ptr(ws1), nbytes,
+                                      reserve_sms, _stream(gemm_stream), _stream(side_stream)),
+           "moe_forward_pipelined")
 
 
 def moe_prepare_backward_weights(L: moe_layer_t, w_down_t: torch.Tensor, s_down_t: torch.Tensor,

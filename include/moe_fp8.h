@@ -90,6 +90,25 @@ int moe_last_cuda_error(void);
 /* Number of kernels this process has launched through the library. */
 uint64_t moe_kernel_launches(void);
 
+/* Limit, in SM clock cycles, of every wait inside the grouped GEMMs'
+ * pipelines (a stage of operands, a TMEM buffer, a slot of scales, the next
+ * tile) for the launches made after this call, by any thread; cycles <= 0
+ * restores the default of 4e9 (about 2 s).  A wait that runs out records
+ * MOE_ERR_TIMEOUT in the call's status word; the kernel then stops, waits
+ * (with the long limit) for its copies and MMAs in flight, releases its
+ * tensor memory and returns, so the context stays usable.  Returns the
+ * previous limit.  A diagnostic of the failure path (no counterpart in the
+ * pages): a limit of a few hundred cycles makes the first wait run out. */
+long long moe_set_pipeline_wait_limit(long long cycles);
+
+/* Test switch of the same failure path (no counterpart in the pages): with
+ * on != 0 the grouped GEMMs launched afterwards issue no operand loads, so
+ * their first pipeline waits run out after the wait limit and the calls
+ * report MOE_ERR_TIMEOUT in their status word; on = 0 restores normal
+ * operation.  Returns the previous setting.  Only for tests of the timeout
+ * path; results of the affected calls are incomplete. */
+int moe_set_pipeline_stall(int on);
+
 /* Workspace bytes moe_forward needs for up to T_max tokens of layer L
  * (0 if L is invalid).  The same workspace serves moe_route and
  * moe_permute at the same T. */
@@ -336,6 +355,25 @@ typedef struct moe_batch_buffers_t {
 int moe_forward_host(const moe_layer_t* L, int T, int n_batches, const uint16_t* const* u_host,
                      float* const* h_host, float gamma, const moe_batch_buffers_t* buf, void* ws,
                      size_t ws_bytes, void* compute_stream, void* h2d_stream, void* d2h_stream);
+
+/* Two micro-batches in flight on one GPU ([YLY] §4.4 inference deployment:
+ * the computation of one micro-batch overlaps the dispatch and combine work
+ * of the other).  The layer over n_batches device-resident batches of T
+ * tokens (batches[k].u in, batches[k].h and the routing out, as moe_forward),
+ * with the bias stepped by moe_update_bias after each batch when gamma != 0.
+ * Batch k's routing, dispatch and quantisation (side_stream) run while batch
+ * k-1's expert GEMMs run (gemm_stream), and batch k-1's combine while batch
+ * k's GEMMs run; the GEMMs' persistent grids leave reserve_sms SMs free for
+ * the side stream's kernels (0: the GEMMs take every SM and the side work
+ * only fills the gaps).  ws0 and ws1 (moe_workspace_size(L, T) bytes each,
+ * 256-byte aligned) alternate between the batches; each one's status word
+ * collects its batches' device errors.  Results are bit-identical to
+ * moe_forward + moe_update_bias batch after batch.  Nothing synchronises
+ * the host: synchronise side_stream (it holds the last combine) before
+ * reading the outputs. */
+int moe_forward_pipelined(const moe_layer_t* L, int T, int n_batches,
+                          const moe_batch_buffers_t* batches, float gamma, void* ws0, void* ws1,
+                          size_t ws_bytes, int reserve_sms, void* gemm_stream, void* side_stream);
 
 /* Input gradient of the layer (the pages: FP8 also carries part of the
  * gradient propagation, [SYH] FP8 資料格式訓練; they wish for transposed
