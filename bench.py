@@ -280,6 +280,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = wl.CONFIGS[args.workload]
+    if args.tokens:
+        cfg = cfg.with_(T=args.tokens)
     pk = peaks()
     layer = MoELayer.from_config(cfg, dev)
     u = wl.tokens(cfg, dev)
@@ -349,7 +351,7 @@ def run_ours(args, world, rank, local):
     fp8_gemm["peak_source"] = fp8_src
 
     e2e = run_e2e(layer, cfg, dev, max(3, min(args.steps, 50)), world)
-    legs = args.workload == "v3_prefill" and not args.no_legs
+    legs = args.workload == "v3_prefill" and not args.no_legs and not args.tokens
     decode = run_decode(layer, cfg, dev, pk) if legs else None
     backward = run_backward(layer, cfg, dev, pk) if legs else None
     wgrad = run_wgrad(layer, cfg, dev, pk) if legs else None
@@ -787,6 +789,8 @@ def main():
     ap.add_argument("--no-legs", action="store_true",
                     help="only the main workload (no decode, backward, skew, long legs)")
     ap.add_argument("--no-fp8-probe", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (profiling-size decode steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
