@@ -166,6 +166,10 @@ class Step:
             if L.n_groups:
                 lib.moe_route_grouped(self.u, L.centroids, L.bias, L.K, L.n_groups, L.topk_groups,
                                       L.group_topk, ws=self.route_ws, out=self.rout)
+            elif self.T < 256:
+                # below 256 tokens moe_forward sums all logits on CUDA cores: the
+                # kernels of moe_route_noalloc
+                lib.moe_route_noalloc(self.u, L.centroids, L.bias, L.K, out=self.rout)
             else:
                 lib.moe_route(self.u, L.centroids, L.bias, L.K, ws=self.route_ws, out=self.rout)
         elif name == "permute":

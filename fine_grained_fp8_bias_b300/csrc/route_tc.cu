@@ -364,17 +364,25 @@ __device__ __forceinline__ float kth_largest(const float (&z)[NV], int E, int K,
 // results do not.  A token with more than CAND_CAP candidates (degenerate
 // inputs) computes all E logits in the select kernel.
 
-// |u_t|^2 by one warp (lane L takes 8 consecutive elements of every 256).
+// |u_t|^2 by one warp (lane L takes 8 consecutive elements of every 256);
+// eight rows' worth of loads are issued before any is used.
 __device__ __forceinline__ float warp_sumsq_bf16(const uint16_t* ut, int d, int lane) {
     float ss = 0.0f;
-    for (int j = lane * 8; j < d; j += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(ut + j);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int j0 = lane * 8; j0 < d; j0 += 8 * 256) {
+        uint4 v[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
-            const float hi = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
-            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        for (int q = 0; q < 8; ++q)
+            if (j0 + q * 256 < d) v[q] = __ldg(reinterpret_cast<const uint4*>(ut + j0 + q * 256));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (j0 + q * 256 >= d) break;
+            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
+                const float hi = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
+                ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+            }
         }
     }
 #pragma unroll
@@ -941,8 +949,19 @@ int launch_select2(const uint16_t* u, const float* c, const float* bias, const f
             exact_pairs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    // one wave of resident blocks (every block then holds a similar run of pairs)
+    static int per_sm = 0;
+    static size_t per_sm_smem = 0;
+    if (per_sm == 0 || per_sm_smem != smem) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, exact_pairs_kernel, EX_WARPS * 32, smem) !=
+                cudaSuccess || b < 1)
+            b = 1;
+        per_sm = b;
+        per_sm_smem = smem;
+    }
     const long long pairs_max = (long long)T * (E < CAND_CAP ? E : CAND_CAP);
-    const long long want = 4LL * sm_count;
+    const long long want = (long long)per_sm * sm_count;
     const int grid = (int)(pairs_max < want ? (pairs_max > 0 ? pairs_max : 1) : want);
     if ((rc = launch_pdl(exact_pairs_kernel, dim3(grid), dim3(EX_WARPS * 32), smem, st, u, c, T, d, E,
                          (const int32_t*)bucket_cnt, (const int32_t*)bucket, exact)))
