@@ -128,8 +128,11 @@ def test_route_edges(L, orc):
         route_case(L, orc, cfg)
 
 
+# up to 1024 selections one block sorts them (T = 1, 16, 128 at K = 8; 32 x 32 over
+# 1024 experts); beyond, the three chunked kernels
 @pytest.mark.parametrize("T,K,E", [(1, 1, 1), (65, 3, 7), (300, 8, 256), (4096, 8, 256),
-                                   (200, 32, 1024), (129, 6, 64)])
+                                   (200, 32, 1024), (129, 6, 64), (1, 8, 256), (16, 8, 256),
+                                   (128, 8, 256), (129, 8, 256), (32, 32, 1024), (5, 8, 1024)])
 def test_permute_bit_exact(L, orc, T, K, E):
     rng = np.random.default_rng(T * 7 + E)
     pool = np.array([e for e in range(E) if e != 2 or E <= K + 1])   # expert 2 stays empty
@@ -149,9 +152,14 @@ def test_permute_bit_exact(L, orc, T, K, E):
 
 
 def test_permute_bad_index_flagged(L):
+    # the one-block sort (4 selections) and the chunked kernels (1600)
     idx = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     L.moe_permute(idx, 4, status=status)
+    assert L.moe_check_device_status(status) == -7
+    big = torch.randint(0, 64, (200, 8), dtype=torch.int32, device="cuda")
+    big[100, 3] = 64
+    L.moe_permute(big, 64, status=status)
     assert L.moe_check_device_status(status) == -7
 
 
