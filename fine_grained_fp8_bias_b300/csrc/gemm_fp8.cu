@@ -162,6 +162,36 @@ __device__ __forceinline__ uint32_t quant4_rcp(float a, float b, float c, float 
     return lo | (hi << 16);
 }
 
+// 8 x 8 transpose of 16-byte chunks within each octet of lanes (lanes 8q ..
+// 8q + 7).  Before: lane j of the octet holds chunks 0..7 of its own output
+// row in x[0..7].  After: x[c] holds chunk j of the row of octet lane c.
+// Three butterfly stages (lane distance 4, 2, 1), each swapping the
+// off-diagonal sub-blocks of the blocks left by the stage before, so that a
+// store instruction afterwards writes 128 contiguous bytes of four rows
+// instead of 16 bytes of 32 rows.
+__device__ __forceinline__ void octet_transpose(uint32_t (&x)[8][4]) {
+    const int j = threadIdx.x & 7;
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1) {
+        const bool upper = (j & k) != 0;
+#pragma unroll
+        for (int c0 = 0; c0 < 8; ++c0) {
+            if (c0 & k) continue;
+            const int c1 = c0 | k;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t send = upper ? x[c0][w] : x[c1][w];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, k);
+                if (upper) x[c0][w] = recv; else x[c1][w] = recv;
+            }
+        }
+    }
+}
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // The next tile index from the ring (-1: no more tiles); false when the wait
 // gave up.  Single-thread form (MMA issuer) and warp form.
 __device__ __forceinline__ bool take_tile(Ctl* ctl, uint32_t& tpos, int& tile, int32_t* status, long long limit) {
@@ -624,25 +654,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             p.out_scales[(size_t)(half * NB + tl.nt) * p.M_total + grow] = scale;
                     }
                 }
-            } else if (valid && cols_valid && tl.g >= p.f32_group0) {
-                float* dst = p.out2 + (size_t)(grow - p.f32_row0) * p.N + tl.nt * BN + wg * 128;
+            } else if (warp_active && cols_valid) {
+                // Down projection: this thread holds 128 consecutive output columns of
+                // its row.  The lanes of each octet trade 16-byte chunks (octet_transpose)
+                // so that every store writes 128 contiguous bytes of one row per octet.
+                // Octet lane c's row is this warp's row 8 (lane / 8) + c.
+                const int j = lane & 7;
+                const int orow0 = (lane & ~7);              // lane of octet row 0
+                const int col0 = tl.nt * BN + wg * 128;
+                uint32_t vmask = 0;                         // bit c: octet row c is an output row
 #pragma unroll
-                for (int j = 0; j < 128; j += 4)
-                    *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-            } else if (valid && cols_valid) {
-                uint16_t* dst = static_cast<uint16_t*>(p.out) + (size_t)grow * p.N + tl.nt * BN + wg * 128;
+                for (int c = 0; c < 8; ++c) {
+                    const int lr = tl.mt * BM + quarter * 32 + orow0 + c;
+                    if (lr < m_g && g0 + lr < p.M_total) vmask |= 1u << c;
+                }
+                const int grow0 = g0 + tl.mt * BM + quarter * 32 + orow0;
+                uint32_t x[8][4];
+                if (tl.g >= p.f32_group0) {
+                    // float32 rows: 32 chunks of four values, in four octet blocks
 #pragma unroll
-                for (int j = 0; j < 128; j += 8) {
-                    uint4 o;
-                    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
-                    __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
-                    __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
-                    o.x = *reinterpret_cast<uint32_t*>(&b0);
-                    o.y = *reinterpret_cast<uint32_t*>(&b1);
-                    o.z = *reinterpret_cast<uint32_t*>(&b2);
-                    o.w = *reinterpret_cast<uint32_t*>(&b3);
-                    *reinterpret_cast<uint4*>(dst + j) = o;
+                    for (int b = 0; b < 4; ++b) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) x[c][w] = __float_as_uint(acc[b * 32 + c * 4 + w]);
+                        octet_transpose(x);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            if (vmask >> c & 1u) {
+                                float* dst = p.out2 + (size_t)(grow0 + c - p.f32_row0) * p.N + col0 + b * 32 + j * 4;
+                                *reinterpret_cast<uint4*>(dst) = make_uint4(x[c][0], x[c][1], x[c][2], x[c][3]);
+                            }
+                    }
+                } else {
+                    // bf16 rows: 16 chunks of eight values, in two octet blocks
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                x[c][w] = bf16x2_bits(acc[b * 64 + c * 8 + 2 * w], acc[b * 64 + c * 8 + 2 * w + 1]);
+                        octet_transpose(x);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            if (vmask >> c & 1u) {
+                                uint16_t* dst = static_cast<uint16_t*>(p.out) + (size_t)(grow0 + c) * p.N + col0 +
+                                                b * 64 + j * 8;
+                                *reinterpret_cast<uint4*>(dst) = make_uint4(x[c][0], x[c][1], x[c][2], x[c][3]);
+                            }
+                    }
                 }
             }
         }
