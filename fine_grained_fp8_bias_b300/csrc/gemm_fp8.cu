@@ -222,8 +222,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmB0,
                             const __grid_constant__ CUtensorMap tmB1, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    griddep_wait();
-    griddep_launch();
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * SMEM_STAGE);
@@ -237,30 +235,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int KB = p.Kdim / BK;
     const int G = p.G;
 
-    // ---- prologue: barriers, TMEM, tile schedule
+    // ---- prologue.  Barriers, TMEM and the tensor-map prefetch touch only this
+    // CTA's own memory, so they are set up before waiting for the kernel this
+    // launch depends on (programmatic dependent launch); the group offsets are
+    // that kernel's output.
     if (warp == 0) {
-        // tile_start[g] = sum_{g' < g} ceil(m_g' / 128) * NT, one warp scan
-        int carry = 0;
-        for (int base = 0; base <= G; base += 32) {
-            const int g = base + lane;
-            int v = 0;
-            if (g <= G) ctl->go[g] = p.go[g];
-            if (g < G) {
-                const int m = max(0, p.go[g + 1] - p.go[g]);
-                v = (m + BM - 1) / BM * NT;
-            }
-            int incl = v;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            if (g <= G) ctl->tile_start[g] = carry + incl - v;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
         if (lane == 0) {
-            ctl->total_tiles = ctl->tile_start[G];
-            ctl->abort = 0;
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(&ctl->full[s], 1);
                 mbar_init(&ctl->empty[s], 1);
@@ -289,6 +269,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          smem_u32(&ctl->tmem_base)),
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    griddep_wait();
+    griddep_launch();
+    // every thread copies a share of the group offsets (one round of loads
+    // instead of one per 32 groups), then warp 0 scans them:
+    // tile_start[g] = sum_{g' < g} ceil(m_g' / 128) * NT
+    for (int g = threadIdx.x; g <= G; g += NUM_THREADS) ctl->go[g] = p.go[g];
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base <= G; base += 32) {
+            const int g = base + lane;
+            int v = 0;
+            if (g < G) {
+                const int m = max(0, ctl->go[g + 1] - ctl->go[g]);
+                v = (m + BM - 1) / BM * NT;
+            }
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (g <= G) ctl->tile_start[g] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            ctl->total_tiles = ctl->tile_start[G];
+            ctl->abort = 0;
+        }
     }
     tc_fence_before();
     __syncthreads();

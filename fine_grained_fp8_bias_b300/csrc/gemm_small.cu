@@ -171,8 +171,6 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     using C = SmallCfg<MODE>;
     constexpr bool gate_up = MODE != 0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    griddep_wait();
-    griddep_launch();
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     SCtl* ctl = reinterpret_cast<SCtl*>(smem + (size_t)C::STAGES * C::STAGE);
@@ -183,29 +181,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     const int KB = p.Kdim / SK;
     const int G = p.G;
 
+    // Barriers, TMEM and the tensor-map prefetch touch only this CTA's own
+    // memory: set up before waiting for the kernel this launch depends on.
     if (warp == 0) {
-        // tile_start[g] = sum over g' < g of NB * ceil(m_g' / 32)
-        int carry = 0;
-        for (int base = 0; base <= G; base += 32) {
-            const int g = base + lane;
-            int v = 0;
-            if (g <= G) ctl->go[g] = p.go[g];
-            if (g < G) {
-                const int m = max(0, p.go[g + 1] - p.go[g]);
-                v = (m + STOK - 1) / STOK * NB;
-            }
-            int incl = v;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            if (g <= G) ctl->tile_start[g] = carry + incl - v;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
         if (lane == 0) {
-            ctl->total_tiles = ctl->tile_start[G];
-            ctl->abort = 0;
             for (int s = 0; s < C::STAGES; ++s) {
                 mbar_init(&ctl->full[s], 1);
                 mbar_init(&ctl->empty[s], 1);
@@ -234,6 +213,35 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                          smem_u32(&ctl->tmem_base)),
                      "r"(S_TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    griddep_wait();
+    griddep_launch();
+    // the group offsets (the preceding kernel's output) in one round of loads,
+    // then warp 0's scan: tile_start[g] = sum over g' < g of NB * ceil(m_g' / 32)
+    for (int g = threadIdx.x; g <= G; g += S_THREADS) ctl->go[g] = p.go[g];
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base <= G; base += 32) {
+            const int g = base + lane;
+            int v = 0;
+            if (g < G) {
+                const int m = max(0, ctl->go[g + 1] - ctl->go[g]);
+                v = (m + STOK - 1) / STOK * NB;
+            }
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (g <= G) ctl->tile_start[g] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            ctl->total_tiles = ctl->tile_start[G];
+            ctl->abort = 0;
+        }
     }
     tc_fence_before();
     __syncthreads();
