@@ -440,7 +440,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int slot = it % SCALE_SLOTS;
                 const uint32_t ph = (it / SCALE_SLOTS) & 1;
                 bool got = true;
-                if (lane == 0) got = mbar_wait(&ctl->sempty[slot], ph ^ 1, &ctl->abort, p.status, p.wait_cycles);
+                if (lane == 0) {
+                    // The loader usually runs ahead with the ring full.  It shares its
+                    // SM sub-partition with two epilogue warps, so it sleeps between
+                    // polls (at most 64 x 128 ns) before the bounded wait.
+                    for (int spin = 0; spin < 64 && !mbar_test(&ctl->sempty[slot], ph ^ 1); ++spin)
+                        __nanosleep(128);
+                    got = mbar_wait(&ctl->sempty[slot], ph ^ 1, &ctl->abort, p.status, p.wait_cycles);
+                }
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) { ok = false; break; }
                 // 4-byte asynchronous copies; rows outside the group are zero-filled
                 // (source size 0).  One commit group per slab; slab it - SCALE_LAG is
