@@ -76,9 +76,14 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(
 
 // Quantise every token once and write its codes to all the rows the
 // dispatch gave it: routed rows inv_row[t, 0..K) and shared rows
-// T*K + s*T + t.  One warp per token; each lane owns 8 consecutive values of
-// a 256-wide step (a half-warp per 128-wide tile), exactly as
-// quant_1x128_kernel, so codes and scales are the same bits.
+// T*K + s*T + t.  One warp per work item; each lane owns 8 consecutive values
+// of a 256-wide step (a half-warp per 128-wide tile), exactly as
+// quant_1x128_kernel, so codes and scales are the same bits.  A work item is
+// SUB consecutive 256-wide steps of one token: the lanes issue all SUB loads
+// before any reduction, so a warp has SUB x 512 bytes of the token in flight
+// (SUB = 4 for large batches; 1 when there are few tokens, to spread them
+// over more warps).
+template <int SUB>
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, int T, int d, const int32_t* __restrict__ inv_row, int K,
     int S, int M, uint8_t* __restrict__ q, float* __restrict__ scales, int scale_ld,
@@ -89,14 +94,12 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const int warps_per_block = blockDim.x >> 5;
     const int half = lane >> 4;
     const int hl = lane & 15;
-    // one work item = one token's 256-column chunk (two 1x128 tiles), so a
-    // few tokens still spread over many warps
-    const int nch = (d + 255) / 256;
+    const int nch = (d + 256 * SUB - 1) / (256 * SUB);
     const long long items = (long long)T * nch;
     for (long long item = (long long)blockIdx.x * warps_per_block + (threadIdx.x >> 5); item < items;
          item += (long long)gridDim.x * warps_per_block) {
         const int t = (int)(item / nch);
-        const int c0 = (int)(item % nch) * 256;
+        const int c0 = (int)(item % nch) * 256 * SUB;
         // lane j < K holds routed row j of this token, lane K + s shared row s
         int my_row = -1;
         if (lane < K) {
@@ -110,19 +113,26 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
         }
         const int R = K + S;
         const uint16_t* xr = x + (size_t)t * d;
-        {
-            const int col = c0 + half * 128 + hl * 8;
+        uint4 raw[SUB];
+#pragma unroll
+        for (int j = 0; j < SUB; ++j) {
+            const int col = c0 + j * 256 + half * 128 + hl * 8;
+            raw[j] = col < d ? *reinterpret_cast<const uint4*>(xr + col) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < SUB; ++j) {
+            const int col = c0 + j * 256 + half * 128 + hl * 8;
+            if (c0 + j * 256 >= d) break;                 // warp-uniform
             const bool active = col < d;
             float v[8];
             float amax = 0.0f;
-            if (active) {
-                uint4 raw = *reinterpret_cast<const uint4*>(xr + col);
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[2 * i] = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
-                    v[2 * i + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
-                }
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu));
+                v[2 * i + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16));
+            }
+            if (active) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
             }
@@ -135,8 +145,8 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
                 out.x = quant4(v[0], v[1], v[2], v[3], scale);
                 out.y = quant4(v[4], v[5], v[6], v[7], scale);
             }
-            for (int j = 0; j < R; ++j) {
-                const int row = __shfl_sync(0xffffffffu, my_row, j);
+            for (int r = 0; r < R; ++r) {
+                const int row = __shfl_sync(0xffffffffu, my_row, r);
                 if (row < 0) continue;
                 if (active) {
                     *reinterpret_cast<uint2*>(q + (size_t)row * d + col) = out;
@@ -202,9 +212,16 @@ int launch_quant_dispatch(const uint16_t* x, int T, int d, const int32_t* inv_ro
                           cudaStream_t st) {
     if (T == 0) return MOE_OK;
     const int warps = 8;
-    const long long items = (long long)T * ((d + 255) / 256);
+    // four 256-wide steps per work item once there are enough items for every
+    // resident warp (148 SMs x 64 warps)
+    const long long items1 = (long long)T * ((d + 255) / 256);
+    const bool wide = items1 >= 4LL * 148 * 64;
+    const long long items = wide ? (long long)T * ((d + 1023) / 1024) : items1;
     const int blocks = (int)((items + warps - 1) / warps < 148 * 16 ? (items + warps - 1) / warps : 148 * 16);
-    return launch_pdl(quant_dispatch_kernel, dim3(blocks), dim3(warps * 32), 0, st, x, T, d, inv_row,
+    if (wide)
+        return launch_pdl(quant_dispatch_kernel<4>, dim3(blocks), dim3(warps * 32), 0, st, x, T, d,
+                          inv_row, K, S, T * (K + S), q, scales, scale_ld, status);
+    return launch_pdl(quant_dispatch_kernel<1>, dim3(blocks), dim3(warps * 32), 0, st, x, T, d, inv_row,
                       K, S, T * (K + S), q, scales, scale_ld, status);
 }
 
