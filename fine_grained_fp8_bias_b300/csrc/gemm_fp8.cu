@@ -321,8 +321,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // claim the next tile (adjacent claims share a weight panel, so
                 // CTAs that claim them together stream it from HBM once) and
                 // publish it to the other roles
-                int next = p.counter ? atomicAdd(p.counter, 1)
-                                     : (tile < 0 ? (int)blockIdx.x : tile + (int)gridDim.x);
+                // the first tile of every CTA is its own index (no atomic on the way
+                // to the first load); later ones come from the counter, which
+                // hands out the tiles from gridDim.x on
+                int next = tile < 0 ? (int)blockIdx.x
+                                    : (p.counter ? (int)gridDim.x + atomicAdd(p.counter, 1)
+                                                 : tile + (int)gridDim.x);
                 if (next >= total_tiles) next = -1;
                 const int slot = tpos % TILE_SLOTS;
                 if (!mbar_wait(&ctl->tile_empty[slot], ((tpos / TILE_SLOTS) & 1) ^ 1, &ctl->abort,

@@ -255,8 +255,12 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             uint32_t it = 0, tpos = 0;
             int tile = -1;
             for (bool ok = true; ok;) {
-                int next = p.counter ? atomicAdd(p.counter, 1)
-                                     : (tile < 0 ? (int)blockIdx.x : tile + (int)gridDim.x);
+                // the first tile of every CTA is its own index (no atomic on the way
+                // to the first load); later ones come from the counter, which
+                // hands out the tiles from gridDim.x on
+                int next = tile < 0 ? (int)blockIdx.x
+                                    : (p.counter ? (int)gridDim.x + atomicAdd(p.counter, 1)
+                                                 : tile + (int)gridDim.x);
                 if (next >= total_tiles) next = -1;
                 const int slot = tpos % S_TILE_SLOTS;
                 if (!mbar_wait(&ctl->tile_empty[slot], ((tpos / S_TILE_SLOTS) & 1) ^ 1, &ctl->abort,
@@ -421,19 +425,30 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
                 const SScaleSlot& sl = ctl->scales[slot];
-                // acc[t] = fma(partial, sa[t] * sw, acc[t])
-                fma2_rowcol<STOK>(acc0, a, sl.sw[0], sl.sa);
-                if (gate_up) fma2_rowcol<STOK>(acc1, b, sl.sw[1], sl.sa);
+                // acc[t] = fma(partial, sa[t] * sw, acc[t]) for the chunk's rows
+                // (nv is the same in every thread: at most 8, 16 or 32 columns)
+                if (nv <= 8) {
+                    fma2_rowcol<8>(acc0, a, sl.sw[0], sl.sa);
+                    if (gate_up) fma2_rowcol<8>(acc1, b, sl.sw[1], sl.sa);
+                } else if (nv <= 16) {
+                    fma2_rowcol<16>(acc0, a, sl.sw[0], sl.sa);
+                    if (gate_up) fma2_rowcol<16>(acc1, b, sl.sw[1], sl.sa);
+                } else {
+                    fma2_rowcol<STOK>(acc0, a, sl.sw[0], sl.sa);
+                    if (gate_up) fma2_rowcol<STOK>(acc1, b, sl.sw[1], sl.sa);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
             }
             if (!ok) break;
             if constexpr (gate_up) {
                 // h = SiLU(g) * u, SiLU(g) = g / (1 + e^-g); amax of each row over
-                // the tile's 128 intermediate indices (the four warps' lanes)
+                // the tile's 128 intermediate indices (the four warps' lanes); only
+                // the chunk's nv rows (nv is the same in every thread)
                 const int par = tcount & 1;
 #pragma unroll
                 for (int t = 0; t < STOK; ++t) {
+                    if (t >= nv) break;
                     const float gv = acc0[t];
                     const float h = __fdiv_rn(gv, 1.0f + expf(-gv)) * acc1[t];
                     acc0[t] = h;
