@@ -11,8 +11,10 @@
 //   hist:    per-chunk histogram of expert ids (shared-memory atomics),
 //   scan:    per-expert totals, exclusive scan -> offsets, and each chunk's
 //            first row per expert,
-//   scatter: each thread owns an expert and walks the chunk's selections in
-//            (token, slot) order, handing out consecutive rows.
+//   scatter: the chunk's selections in (token, slot) order are split into
+//            eight runs, one per warp; each warp's rows per expert start after
+//            the earlier warps', and within a run the lanes holding the same
+//            expert are ranked by lane.
 #include "common.cuh"
 
 namespace moe {
@@ -92,34 +94,69 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
 }
 
 // Also writes the rows of the S shared-expert groups: row T*K + s*T + t is
-// token t.
-__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ idx, int T,
+// token t.  The chunk's selections, in (token, slot) order, are cut into
+// eight consecutive runs, one per warp.  Each warp counts its run's experts;
+// the counts are turned into each warp's first row per expert (the chunk's
+// base plus the earlier warps' counts, one thread per expert); then each warp
+// walks its run 32 selections at a time, the lanes holding the same expert
+// ranked by lane (__match_any_sync), and advances its rows by their number.
+// Rows of one expert thus ascend in selection order, as the layout requires.
+constexpr int SCAT_WARPS = 8;
+__global__ void __launch_bounds__(SCAT_WARPS * 32) scatter_kernel(const int32_t* __restrict__ idx, int T,
                                                       int K, int E, int S,
                                                       const int32_t* __restrict__ base,
                                                       int32_t* __restrict__ perm,
                                                       int32_t* __restrict__ inv_row) {
-    extern __shared__ int32_t sel[];            // this chunk's selections, (token, slot) order
+    extern __shared__ int32_t smem_scat[];
+    int32_t* sel = smem_scat;                        // [kPermuteChunk * K] the chunk's selections
+    int32_t* wrow = smem_scat + kPermuteChunk * K;   // [SCAT_WARPS][E] counts, then first rows
     griddep_wait();
     griddep_launch();
     const int t0 = blockIdx.x * kPermuteChunk;
     const int t1 = min(T, t0 + kPermuteChunk);
     const int n = (t1 - t0) * K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int p = threadIdx.x; p < S * (t1 - t0); p += blockDim.x) {
         const int s = p / (t1 - t0), t = t0 + p % (t1 - t0);
         perm[(size_t)T * K + (size_t)s * T + t] = t;
     }
     for (int p = threadIdx.x; p < n; p += blockDim.x) sel[p] = idx[(size_t)t0 * K + p];
+    for (int i = threadIdx.x; i < SCAT_WARPS * E; i += blockDim.x) wrow[i] = 0;
+    __syncthreads();
+    // this warp's run of selections: [p0, p1), whole steps of 32 lanes
+    const int per = ((n + SCAT_WARPS - 1) / SCAT_WARPS + 31) / 32 * 32;
+    const int p0 = min(n, warp * per), p1 = min(n, p0 + per);
+    int32_t* myrow = wrow + warp * E;
+    for (int p = p0 + lane; p < p1; p += 32) {
+        const int e = sel[p];
+        if (e >= 0 && e < E) atomicAdd(&myrow[e], 1);
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int row = base[(size_t)blockIdx.x * E + e];
-        for (int p = 0; p < n; ++p) {
-            if (sel[p] == e) {
-                const int t = t0 + p / K;
-                perm[row] = t;
-                inv_row[(size_t)t0 * K + p] = row;
-                ++row;
-            }
+        int run = base[(size_t)blockIdx.x * E + e];
+        for (int w = 0; w < SCAT_WARPS; ++w) {
+            const int c = wrow[w * E + e];
+            wrow[w * E + e] = run;
+            run += c;
         }
+    }
+    __syncthreads();
+    for (int q0 = p0; q0 < p1; q0 += 32) {
+        const int p = q0 + lane;
+        const bool have = p < p1;
+        const int e = have ? sel[p] : -1;
+        const bool ok = have && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (ok) {
+            const int row = myrow[e] + rank;
+            perm[row] = t0 + p / K;
+            inv_row[(size_t)t0 * K + p] = row;
+        }
+        __syncwarp();
+        // the lowest lane of each expert's peers advances that expert's rows
+        if (ok && rank == 0) myrow[e] += __popc(peers);
+        __syncwarp();
     }
 }
 
@@ -223,9 +260,9 @@ int launch_permute(const int32_t* idx, int T, int K, int E, int32_t* offsets, in
                          E, T, K, S, ws_base, offsets, go_ext)))
         return rc;
     if (nchunks > 0)
-        rc = launch_pdl(scatter_kernel, dim3(nchunks), dim3(256),
-                        sizeof(int32_t) * kPermuteChunk * K, st, idx, T, K, E, S,
-                        (const int32_t*)ws_base, perm, inv_row);
+        rc = launch_pdl(scatter_kernel, dim3(nchunks), dim3(SCAT_WARPS * 32),
+                        sizeof(int32_t) * ((size_t)kPermuteChunk * K + (size_t)SCAT_WARPS * E), st,
+                        idx, T, K, E, S, (const int32_t*)ws_base, perm, inv_row);
     return rc;
 }
 
