@@ -259,9 +259,10 @@ int moe_permute(const int32_t* topk_idx, int T, int K, int E, int S, int32_t* of
  * G <= 1088; all pointers 16-byte aligned.  status (device int32 [2],
  * nullable): status[0] receives MOE_ERR_TIMEOUT if a pipeline wait ran out
  * (the kernel then stops early and its output is incomplete); status[1] is
- * the call's tile counter (cleared by the call; the CTAs claim output tiles
- * from it in order, so tiles that share a weight panel run together).
- * Without a status buffer the tiles are taken in a fixed order. */
+ * the call's tile counter (cleared by the call).  Each CTA's first output
+ * tile is the one numbered like the CTA; the later tiles are claimed from the
+ * counter in order, so tiles that share a weight panel run together.
+ * Without a status buffer every CTA takes every grid-th tile. */
 int moe_grouped_gemm_fp8(int mode, const uint8_t* A, const float* sa, int M_total,
                          const int32_t* group_offsets, int G, const uint8_t* W0,
                          const uint8_t* W1, const float* sw0, const float* sw1, int N, int Kdim,
