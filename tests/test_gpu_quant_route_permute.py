@@ -174,7 +174,11 @@ def test_update_bias_bit_exact(L, orc):
     assert np.array_equal(bd.cpu().numpy(), orc.update_bias(counts, b.numpy(), T, K, 1e-3))
 
 
-@pytest.mark.parametrize("T,K,S,E,d", [(1, 1, 1, 4, 128), (97, 3, 2, 16, 384), (300, 8, 1, 64, 2048)])
+# The last two cases have at least 148 * 64 * 4 = 37888 256-wide steps, so the
+# kernel takes four steps of a token per warp item; the last one's d (65 tiles
+# of 128) leaves a partly filled final item.
+@pytest.mark.parametrize("T,K,S,E,d", [(1, 1, 1, 4, 128), (97, 3, 2, 16, 384), (300, 8, 1, 64, 2048),
+                                       (2600, 8, 1, 64, 4096), (1200, 2, 1, 16, 8320)])
 def test_quant_dispatch_bit_exact(L, orc, T, K, S, E, d):
     rng = np.random.default_rng(T + d)
     idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
